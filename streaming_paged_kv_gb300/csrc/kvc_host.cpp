@@ -1,0 +1,679 @@
+// Host side of libkvc.so: the page allocator (scale / live / free deques of
+// patch page IDs per block), the special-stream counters, the undo stack for
+// rollback, plan construction and the C ABI declared in include/kvc.h.
+//
+// Pages cited by tag, then section:
+//   [KVC]   "How LingBot-Map Implements the KV Cache Mechanism for Streaming
+//           Inference with FlashInfer Integration"
+//   [PERF]  "How to Improve Streaming Inference Performance with FlashInfer KV
+//           Cache Backend"
+//   [SLOTS] "LingBot-Map KV缓存机制深度揭秘：scale frames与keyframes如何占用slot"
+//
+// Every buffer the handle uses is allocated in kvc_create; no call after it
+// allocates host or device memory ([PERF] "Two-Stream Page Pool
+// Architecture": pages only move between deques after construction).
+
+#include "kvc.h"
+#include "kvc_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+using kvc::kNumSpecial;
+
+namespace {
+
+// Fixed-capacity ring deque of page IDs.
+struct Ring {
+  int32_t* buf = nullptr;
+  int32_t cap = 0, head = 0, size = 0;
+  void bind(int32_t* storage, int32_t c) { buf = storage; cap = c; head = 0; size = 0; }
+  void clear() { head = 0; size = 0; }
+  int32_t at(int32_t i) const { return buf[(head + i) % cap]; }
+  int32_t back() const { return buf[(head + size - 1) % cap]; }
+  void push_back(int32_t v) { buf[(head + size) % cap] = v; ++size; }
+  void push_front(int32_t v) { head = (head + cap - 1) % cap; buf[head] = v; ++size; }
+  int32_t pop_front() { int32_t v = buf[head]; head = (head + 1) % cap; --size; return v; }
+  int32_t pop_back() { int32_t v = back(); --size; return v; }
+};
+
+struct Undo {
+  int32_t page;
+  int32_t to_scale;
+};
+
+struct Block {
+  Ring scale, live, free_list;
+  int32_t special_frames = 0;  // frames in the special stream
+  int32_t frame_count = 0;
+  Undo* undo = nullptr;        // uncommitted appends, newest last
+  int32_t n_undo = 0;
+
+  // Construction state: all patch pages free, in ID order.
+  void reset(int32_t P) {
+    scale.clear();
+    live.clear();
+    free_list.clear();
+    for (int32_t i = 0; i < P; ++i) free_list.push_back(i);
+    special_frames = 0;
+    frame_count = 0;
+    n_undo = 0;
+  }
+};
+
+constexpr int kEventPairs = 4096;
+constexpr int kDefaultSplits = 32;
+
+int64_t elem_bytes(int dtype) { return dtype == KVC_F32 ? 4 : 2; }
+
+// Validate cfg and fill defaults.  Returns KVC_OK or INVALID_ARG.
+int resolve(const kvc_config* in, kvc_config* out) {
+  if (!in || !out) return KVC_ERR_INVALID_ARG;
+  kvc_config c = *in;
+  if (c.num_special_tokens == 0) c.num_special_tokens = kNumSpecial;
+  if (c.max_kv_splits == 0) c.max_kv_splits = kDefaultSplits;
+  if (c.max_query_tokens == 0) c.max_query_tokens = kNumSpecial + c.page_size;
+  if (c.sm_scale == 0.0f && c.head_dim > 0) c.sm_scale = 1.0f / std::sqrt((float)c.head_dim);
+  if (c.num_blocks < 1 || c.num_heads < 1 || c.num_heads > 4096) return KVC_ERR_INVALID_ARG;
+  if (c.head_dim != 32 && c.head_dim != 64 && c.head_dim != 128) return KVC_ERR_INVALID_ARG;
+  if (c.dtype < KVC_BF16 || c.dtype > KVC_F32) return KVC_ERR_INVALID_ARG;
+  if (c.num_special_tokens != kNumSpecial) return KVC_ERR_INVALID_ARG;
+  if (c.page_size < kNumSpecial || c.page_size > (1 << 16)) return KVC_ERR_INVALID_ARG;
+  if (c.scale_frames < 0 || c.sliding_window < 0 || c.headroom < 0) return KVC_ERR_INVALID_ARG;
+  int64_t P = (int64_t)c.scale_frames + c.sliding_window + c.headroom;
+  if (P < 1 || P > kvc::kMaxPatchPages) return KVC_ERR_INVALID_ARG;
+  if (c.max_total_frames < 1 || c.max_total_frames > (1 << 24)) return KVC_ERR_INVALID_ARG;
+  if (c.max_query_tokens < 1 || c.max_query_tokens > (1 << 20)) return KVC_ERR_INVALID_ARG;
+  if (c.max_kv_splits < 1 || c.max_kv_splits > 256) return KVC_ERR_INVALID_ARG;
+  if (!(c.sm_scale > 0.0f) || !std::isfinite(c.sm_scale)) return KVC_ERR_INVALID_ARG;
+  if (((int64_t)c.num_heads * c.head_dim * elem_bytes(c.dtype)) % 16 != 0) return KVC_ERR_INVALID_ARG;
+  *out = c;
+  return KVC_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Geometry {
+  int32_t P, fpp, n_special_pages, max_pages, T;
+  int64_t row_bytes, page_bytes, block_bytes;
+  size_t cache_bytes;
+  kvc::WorkspaceLayout L;
+};
+
+void geometry(const kvc_config& c, Geometry* g) {
+  g->P = c.scale_frames + c.sliding_window + c.headroom;
+  g->fpp = c.page_size / kNumSpecial;                      // floor(page_size / 6)
+  g->n_special_pages = (c.max_total_frames + g->fpp - 1) / g->fpp;
+  g->max_pages = g->P + g->n_special_pages;
+  g->T = kNumSpecial + c.page_size;
+  g->row_bytes = (int64_t)c.num_heads * c.head_dim * elem_bytes(c.dtype);
+  g->page_bytes = 2 * (int64_t)c.page_size * g->row_bytes;  // K and V of one page
+  g->block_bytes = (int64_t)g->max_pages * g->page_bytes;
+  g->cache_bytes = (size_t)g->block_bytes * c.num_blocks;
+  // The smallest tile any attention kernel uses bounds the tile count.
+  const int min_rows = 32;
+  int64_t max_tiles = (int64_t)g->max_pages * ((c.page_size + min_rows - 1) / min_rows);
+  kvc::WorkspaceLayout& L = g->L;
+  size_t off = 0;
+  L.status = off;   off += 256;
+  L.header = off;   off += 256;
+  L.page_ids = off; off = align_up(off + 4 * (size_t)g->max_pages, 256);
+  L.page_valid = off; off = align_up(off + 4 * (size_t)g->max_pages, 256);
+  L.tiles = off;    off = align_up(off + sizeof(kvc::KvTile) * (size_t)max_tiles, 256);
+  L.part_o = off;
+  off = align_up(off + 4 * (size_t)c.max_kv_splits * c.max_query_tokens * c.num_heads * c.head_dim, 256);
+  L.part_lse = off;
+  off = align_up(off + 4 * (size_t)c.max_kv_splits * c.max_query_tokens * c.num_heads, 256);
+  L.total = off;
+  L.max_pages = g->max_pages;
+  L.max_tiles = (int32_t)max_tiles;
+}
+
+}  // namespace
+
+struct kvc_handle {
+  kvc_config cfg;
+  Geometry g;
+  char* cache = nullptr;      // borrowed device buffers
+  char* ws = nullptr;
+  bool device = false;
+  int num_sms = 0;
+  Block* blocks = nullptr;
+  int32_t* ring_storage = nullptr;
+  Undo* undo_storage = nullptr;
+  bool defer = false;
+  // Plan (host copy + the state it was made from).
+  bool has_plan = false;
+  int32_t plan_n_pages = 0, plan_lpl = 0, plan_n_tiles = 0, plan_tile_rows = 0, plan_kernel = 0;
+  int32_t plan_n_scale = 0, plan_n_live = 0, plan_special_frames = 0;
+  int32_t* plan_ids = nullptr;      // [max_pages]
+  int32_t* plan_snapshot = nullptr; // [P]: scale then live
+  kvc::PlanArgs* plan_args = nullptr;
+  // Options.
+  int opt_kernel = 0;
+  int opt_splits = 0;
+  long long wait_budget = 0;
+  bool timing = false;
+  // Counters.
+  int64_t launches = 0, attn_launches = 0;
+  double attn_ms = 0.0;
+  cudaEvent_t* ev = nullptr;        // [2 * kEventPairs] when timing
+  bool* ev_used = nullptr;
+  int ev_next = 0;
+  kvc::TcMaps* maps = nullptr;
+};
+
+namespace {
+
+int check_block(const kvc_handle* h, int32_t block) {
+  if (!h || block < 0 || block >= h->cfg.num_blocks) return KVC_ERR_INVALID_ARG;
+  return KVC_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Move live pages to the free list until at most `window` remain; an eviction
+// that moves a page commits the block's pending frames.
+int32_t evict_to(Block& b, int32_t window, bool commit_always) {
+  int32_t moved = 0;
+  while (b.live.size > window) {
+    b.free_list.push_back(b.live.pop_front());
+    ++moved;
+  }
+  if (moved || commit_always) b.n_undo = 0;
+  return moved;
+}
+
+int attn_kernel_for(const kvc_handle* h) {
+  const kvc_config& c = h->cfg;
+  bool tc = h->maps != nullptr && kvc::tc_supported(c.dtype, c.head_dim, c.num_heads, c.page_size);
+  if (h->opt_kernel == 1) return 1;
+  if (h->opt_kernel == 2) return tc ? 2 : -1;
+  return tc ? 2 : 1;
+}
+
+int tile_rows_for(const kvc_handle* h, int kernel) {
+  return kernel == 2 ? kvc::kTcTileRows : kvc::simt_tile_rows(h->cfg.head_dim);
+}
+
+// Number of KV splits: balance waves of CTAs against work per split, with a
+// small charge per split for the merge.
+int choose_splits(const kvc_handle* h, int kernel, int32_t n_q) {
+  int max_s = h->cfg.max_kv_splits;
+  if (max_s > h->plan_n_tiles) max_s = h->plan_n_tiles;
+  if (max_s < 1) max_s = 1;
+  if (h->opt_splits > 0) return h->opt_splits < max_s ? h->opt_splits : max_s;
+  int q_rows = kernel == 2 ? kvc::kTcQRows : 128;
+  int64_t base = (int64_t)((n_q + q_rows - 1) / q_rows) * h->cfg.num_heads;
+  int64_t slots = (int64_t)h->num_sms * (kernel == 2 ? 1 : 2);
+  double best = 1e300;
+  int best_s = 1;
+  for (int s = 1; s <= max_s; ++s) {
+    int64_t waves = (base * s + slots - 1) / slots;
+    int64_t per = (h->plan_n_tiles + s - 1) / s;
+    double cost = (double)waves * per * (1.0 + (s > 1 ? 0.02 * s : 0.0));
+    if (cost < best - 1e-9) { best = cost; best_s = s; }
+  }
+  return best_s;
+}
+
+void record_timing(kvc_handle* h, int which, cudaStream_t st) {
+  // which 0: start, 1: stop of the current pair.
+  int i = h->ev_next;
+  if (which == 0 && h->ev_used[i]) {
+    float ms = 0.f;
+    cudaEventSynchronize(h->ev[2 * i + 1]);
+    if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) == cudaSuccess) h->attn_ms += ms;
+    h->ev_used[i] = false;
+  }
+  cudaEventRecord(h->ev[2 * i + which], st);
+  if (which == 1) {
+    h->ev_used[i] = true;
+    h->ev_next = (i + 1) % kEventPairs;
+  }
+}
+
+void drain_timing(kvc_handle* h) {
+  if (!h->ev) return;
+  for (int i = 0; i < kEventPairs; ++i) {
+    if (!h->ev_used[i]) continue;
+    float ms = 0.f;
+    cudaEventSynchronize(h->ev[2 * i + 1]);
+    if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) == cudaSuccess) h->attn_ms += ms;
+    h->ev_used[i] = false;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvc_required_bytes(const kvc_config* cfg, size_t* cache_bytes, size_t* workspace_bytes) {
+  kvc_config c;
+  int rc = resolve(cfg, &c);
+  if (rc) return rc;
+  Geometry g;
+  geometry(c, &g);
+  if (cache_bytes) *cache_bytes = g.cache_bytes;
+  if (workspace_bytes) *workspace_bytes = g.L.total;
+  return KVC_OK;
+}
+
+int kvc_create(const kvc_config* cfg, void* cache_dev, void* workspace_dev, kvc_stream stream,
+               kvc_handle** out) {
+  if (!out) return KVC_ERR_INVALID_ARG;
+  *out = nullptr;
+  kvc_config c;
+  int rc = resolve(cfg, &c);
+  if (rc) return rc;
+  if ((cache_dev == nullptr) != (workspace_dev == nullptr)) return KVC_ERR_INVALID_ARG;
+  if (((uintptr_t)cache_dev & 255u) || ((uintptr_t)workspace_dev & 255u)) return KVC_ERR_INVALID_ARG;
+  kvc_handle* h = new (std::nothrow) kvc_handle();
+  if (!h) return KVC_ERR_INVALID_ARG;
+  h->cfg = c;
+  geometry(c, &h->g);
+  const int32_t P = h->g.P;
+  h->blocks = new (std::nothrow) Block[c.num_blocks];
+  h->ring_storage = (int32_t*)std::calloc((size_t)c.num_blocks * 3 * P, sizeof(int32_t));
+  h->undo_storage = (Undo*)std::calloc((size_t)c.num_blocks * P, sizeof(Undo));
+  h->plan_ids = (int32_t*)std::calloc((size_t)h->g.max_pages, sizeof(int32_t));
+  h->plan_snapshot = (int32_t*)std::calloc((size_t)P, sizeof(int32_t));
+  h->plan_args = (kvc::PlanArgs*)std::calloc(1, sizeof(kvc::PlanArgs));
+  if (!h->blocks || !h->ring_storage || !h->undo_storage || !h->plan_ids || !h->plan_snapshot ||
+      !h->plan_args) {
+    kvc_destroy(h);
+    return KVC_ERR_INVALID_ARG;
+  }
+  for (int b = 0; b < c.num_blocks; ++b) {
+    Block& B = h->blocks[b];
+    int32_t* base = h->ring_storage + (size_t)b * 3 * P;
+    B.scale.bind(base, P);
+    B.live.bind(base + P, P);
+    B.free_list.bind(base + 2 * P, P);
+    B.undo = h->undo_storage + (size_t)b * P;
+    B.reset(P);
+  }
+  if (cache_dev) {
+    h->device = true;
+    h->cache = (char*)cache_dev;
+    h->ws = (char*)workspace_dev;
+    int dev = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaMemsetAsync(h->cache, 0, h->g.cache_bytes, st) != cudaSuccess ||
+        cudaMemsetAsync(h->ws, 0, h->g.L.part_o, st) != cudaSuccess) {
+      kvc_destroy(h);
+      return KVC_ERR_CUDA;
+    }
+    if (kvc::tc_supported(c.dtype, c.head_dim, c.num_heads, c.page_size)) {
+      cudaError_t err = cudaSuccess;
+      h->maps = kvc::tc_create_maps(h->cache, c.dtype, c.num_blocks, h->g.max_pages, c.page_size,
+                                    c.num_heads, c.head_dim, &err);
+      if (!h->maps) {
+        kvc_destroy(h);
+        return KVC_ERR_CUDA;
+      }
+    }
+  }
+  *out = h;
+  return KVC_OK;
+}
+
+int kvc_destroy(kvc_handle* h) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (h->ev) {
+    for (int i = 0; i < 2 * kEventPairs; ++i)
+      if (h->ev[i]) cudaEventDestroy(h->ev[i]);
+    std::free(h->ev);
+  }
+  std::free(h->ev_used);
+  if (h->maps) kvc::tc_destroy_maps(h->maps);
+  delete[] h->blocks;
+  std::free(h->ring_storage);
+  std::free(h->undo_storage);
+  std::free(h->plan_ids);
+  std::free(h->plan_snapshot);
+  std::free(h->plan_args);
+  delete h;
+  return KVC_OK;
+}
+
+int kvc_append_frame(kvc_handle* h, int32_t block, const void* K, const void* V, kvc_stream stream) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  if (h->device ? (!K || !V || !aligned16(K) || !aligned16(V)) : (K || V)) return KVC_ERR_INVALID_ARG;
+  Block& b = h->blocks[block];
+  if (b.special_frames >= h->cfg.max_total_frames) return KVC_ERR_SPECIAL_POOL_FULL;
+  if (b.free_list.size == 0) return KVC_ERR_NO_FREE_PAGE;
+  // Where this frame's tokens go.
+  const int32_t page = b.free_list.at(0);
+  const int32_t s = b.special_frames;
+  const int32_t sp_page = h->g.P + s / h->g.fpp;
+  const int32_t sp_slot = kNumSpecial * (s % h->g.fpp);
+  if (h->device) {
+    char* cache_block = h->cache + (size_t)block * h->g.block_bytes;
+    cudaError_t err = kvc::launch_append(cache_block, K, V, page, sp_page, sp_slot, h->cfg.page_size,
+                                         h->g.row_bytes, (cudaStream_t)stream);
+    if (err != cudaSuccess) return KVC_ERR_CUDA;
+    ++h->launches;
+  }
+  // Commit the bookkeeping only once the copy is enqueued.
+  b.free_list.pop_front();
+  const bool to_scale = b.scale.size < h->cfg.scale_frames;   // _write_patch_page routing
+  if (to_scale) b.scale.push_back(page); else b.live.push_back(page);
+  b.undo[b.n_undo++] = Undo{page, to_scale ? 1 : 0};
+  b.special_frames = s + 1;
+  b.frame_count += 1;
+  return KVC_OK;
+}
+
+int kvc_evict_frames(kvc_handle* h, int32_t block, int32_t scale_frames, int32_t sliding_window) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  if (scale_frames != h->cfg.scale_frames || sliding_window < 0) return KVC_ERR_INVALID_ARG;
+  if (h->defer) return KVC_OK;
+  evict_to(h->blocks[block], sliding_window, false);
+  return KVC_OK;
+}
+
+int kvc_set_defer_eviction(kvc_handle* h, int32_t on) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  h->defer = on != 0;
+  return KVC_OK;
+}
+
+int kvc_execute_deferred_eviction(kvc_handle* h, int32_t block, int32_t scale_frames,
+                                  int32_t sliding_window) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  if (scale_frames != h->cfg.scale_frames || sliding_window < 0) return KVC_ERR_INVALID_ARG;
+  evict_to(h->blocks[block], sliding_window, true);
+  return KVC_OK;
+}
+
+int kvc_rollback_last_frame(kvc_handle* h, int32_t block) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  Block& b = h->blocks[block];
+  if (b.n_undo == 0) return KVC_ERR_NOTHING_TO_ROLLBACK;
+  const Undo u = b.undo[b.n_undo - 1];
+  Ring& region = u.to_scale ? b.scale : b.live;
+  if (region.size == 0 || region.back() != u.page) return KVC_ERR_ROLLBACK_AFTER_EVICT;
+  region.pop_back();
+  b.free_list.push_front(u.page);
+  b.n_undo -= 1;
+  b.special_frames -= 1;
+  b.frame_count -= 1;
+  return KVC_OK;
+}
+
+int kvc_clean(kvc_handle* h) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  for (int b = 0; b < h->cfg.num_blocks; ++b) h->blocks[b].reset(h->g.P);
+  h->defer = false;
+  h->has_plan = false;
+  return KVC_OK;
+}
+
+int kvc_plan(kvc_handle* h, kvc_stream stream) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  const Block& b = h->blocks[0];
+  const int32_t fpp = h->g.fpp;
+  const int32_t s = b.special_frames;
+  const int32_t n_sp = (s + fpp - 1) / fpp;
+  const int32_t n_patch = b.scale.size + b.live.size;
+  const int32_t n_pages = n_patch + n_sp;
+  if (n_pages == 0) return KVC_ERR_EMPTY;
+  // Tokens in the last special page (compute_last_page_len).
+  const int32_t lpl = n_sp > 0 ? kNumSpecial * (s - fpp * (n_sp - 1)) : h->cfg.page_size;
+  const int kernel = h->device ? attn_kernel_for(h) : 1;
+  if (kernel < 0) return KVC_ERR_INVALID_ARG;
+  const int32_t tr = tile_rows_for(h, kernel);
+  // Tiles: ceil(valid / tile_rows) per visible page.
+  const int32_t full_sp = kNumSpecial * fpp;
+  int64_t n_tiles = (int64_t)n_patch * ((h->cfg.page_size + tr - 1) / tr);
+  if (n_sp > 0) n_tiles += (int64_t)(n_sp - 1) * ((full_sp + tr - 1) / tr) + (lpl + tr - 1) / tr;
+  if (n_tiles > h->g.L.max_tiles) return KVC_ERR_INVALID_ARG;
+  kvc::PlanArgs& a = *h->plan_args;
+  a.n_patch = n_patch;
+  a.n_special = n_sp;
+  a.first_special = h->g.P;
+  a.full_special_len = full_sp;
+  a.last_page_len = lpl;
+  a.page_size = h->cfg.page_size;
+  a.tile_rows = tr;
+  for (int32_t i = 0; i < b.scale.size; ++i) a.patch_ids[i] = b.scale.at(i);
+  for (int32_t i = 0; i < b.live.size; ++i) a.patch_ids[b.scale.size + i] = b.live.at(i);
+  if (h->device) {
+    cudaError_t err = kvc::launch_plan(a, h->ws, h->g.L, (cudaStream_t)stream);
+    if (err != cudaSuccess) return KVC_ERR_CUDA;
+    ++h->launches;
+  }
+  // Host copy of the plan and of the state it describes.
+  for (int32_t i = 0; i < n_patch; ++i) h->plan_ids[i] = a.patch_ids[i];
+  for (int32_t i = 0; i < n_sp; ++i) h->plan_ids[n_patch + i] = h->g.P + i;
+  for (int32_t i = 0; i < n_patch; ++i) h->plan_snapshot[i] = a.patch_ids[i];
+  h->plan_n_scale = b.scale.size;
+  h->plan_n_live = b.live.size;
+  h->plan_special_frames = s;
+  h->plan_n_pages = n_pages;
+  h->plan_lpl = lpl;
+  h->plan_n_tiles = (int32_t)n_tiles;
+  h->plan_tile_rows = tr;
+  h->plan_kernel = kernel;
+  h->has_plan = true;
+  return KVC_OK;
+}
+
+int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q, kvc_stream stream) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  if (!h->device) return KVC_ERR_NO_DEVICE;
+  if (!h->has_plan) return KVC_ERR_NO_PLAN;
+  if (n_q < 0 || n_q > h->cfg.max_query_tokens) return KVC_ERR_INVALID_ARG;
+  if (n_q > 0 && (!Q || !out || !aligned16(Q) || !aligned16(out))) return KVC_ERR_INVALID_ARG;
+  // The plan is valid for this block only if its pages are the planned ones.
+  const Block& b = h->blocks[block];
+  if (b.scale.size != h->plan_n_scale || b.live.size != h->plan_n_live ||
+      b.special_frames != h->plan_special_frames)
+    return KVC_ERR_STALE_PLAN;
+  for (int32_t i = 0; i < b.scale.size; ++i)
+    if (b.scale.at(i) != h->plan_snapshot[i]) return KVC_ERR_STALE_PLAN;
+  for (int32_t i = 0; i < b.live.size; ++i)
+    if (b.live.at(i) != h->plan_snapshot[b.scale.size + i]) return KVC_ERR_STALE_PLAN;
+  if (n_q == 0) return KVC_OK;
+  const int kernel = h->plan_kernel;
+  const int splits = choose_splits(h, kernel, n_q);
+  kvc::AttnArgs a;
+  a.q = Q;
+  a.out = out;
+  a.cache = h->cache + (size_t)block * h->g.block_bytes;
+  a.tiles = (const kvc::KvTile*)(h->ws + h->g.L.tiles);
+  a.part_o = (float*)(h->ws + h->g.L.part_o);
+  a.part_lse = (float*)(h->ws + h->g.L.part_lse);
+  a.status = (int32_t*)(h->ws + h->g.L.status);
+  a.n_q = n_q;
+  a.num_heads = h->cfg.num_heads;
+  a.head_dim = h->cfg.head_dim;
+  a.page_size = h->cfg.page_size;
+  a.n_tiles = h->plan_n_tiles;
+  a.n_splits = splits;
+  a.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
+  a.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->timing) record_timing(h, 0, st);
+  cudaError_t err = kernel == 2 ? kvc::launch_attn_tc(a, h->maps, block, h->g.max_pages, h->cfg.dtype, st)
+                                : kvc::launch_attn_simt(a, h->cfg.dtype, st);
+  if (h->timing) record_timing(h, 1, st);
+  if (err != cudaSuccess) return KVC_ERR_CUDA;
+  ++h->launches;
+  ++h->attn_launches;
+  if (splits > 1) {
+    err = kvc::launch_merge(a, h->cfg.dtype, st);
+    if (err != cudaSuccess) return KVC_ERR_CUDA;
+    ++h->launches;
+  }
+  return KVC_OK;
+}
+
+int kvc_get_cache_stats(const kvc_handle* h, int32_t block, kvc_stats* out) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  if (!out) return KVC_ERR_INVALID_ARG;
+  const Block& b = h->blocks[block];
+  out->frame_count = b.frame_count;
+  out->scale_pages = b.scale.size;
+  out->live_pages = b.live.size;
+  out->free_pages = b.free_list.size;
+  out->special_tokens = (int64_t)kNumSpecial * b.special_frames;
+  return KVC_OK;
+}
+
+int kvc_get_plan(const kvc_handle* h, int32_t* indptr2, int32_t* indices, int32_t cap,
+                 int32_t* n_pages, int32_t* last_page_len) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (!h->has_plan) return KVC_ERR_NO_PLAN;
+  if (n_pages) *n_pages = h->plan_n_pages;
+  if (last_page_len) *last_page_len = h->plan_lpl;
+  if (indptr2) { indptr2[0] = 0; indptr2[1] = h->plan_n_pages; }
+  if (indices) {
+    if (cap < h->plan_n_pages) return KVC_ERR_INVALID_ARG;
+    std::memcpy(indices, h->plan_ids, sizeof(int32_t) * h->plan_n_pages);
+  }
+  return KVC_OK;
+}
+
+int kvc_get_deques(const kvc_handle* h, int32_t block, int32_t* scale, int32_t* n_scale,
+                   int32_t* live, int32_t* n_live, int32_t* free_list, int32_t* n_free) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  const Block& b = h->blocks[block];
+  if (n_scale) *n_scale = b.scale.size;
+  if (n_live) *n_live = b.live.size;
+  if (n_free) *n_free = b.free_list.size;
+  if (scale) for (int32_t i = 0; i < b.scale.size; ++i) scale[i] = b.scale.at(i);
+  if (live) for (int32_t i = 0; i < b.live.size; ++i) live[i] = b.live.at(i);
+  if (free_list) for (int32_t i = 0; i < b.free_list.size; ++i) free_list[i] = b.free_list.at(i);
+  return KVC_OK;
+}
+
+int kvc_read_device_plan(kvc_handle* h, int32_t* indices, int32_t* valid_lens, int32_t cap,
+                         int32_t* n_pages, int32_t* last_page_len, kvc_stream stream) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (!h->device) return KVC_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  kvc::DevPlanHeader hd;
+  if (cudaMemcpyAsync(&hd, h->ws + h->g.L.header, sizeof(hd), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (n_pages) *n_pages = hd.n_pages;
+  if (last_page_len) *last_page_len = hd.last_page_len;
+  if (hd.n_pages < 0 || hd.n_pages > h->g.max_pages) return KVC_ERR_INVALID_ARG;
+  if ((indices || valid_lens) && cap < hd.n_pages) return KVC_ERR_INVALID_ARG;
+  if (hd.n_pages > 0) {
+    if (indices && cudaMemcpyAsync(indices, h->ws + h->g.L.page_ids, 4 * (size_t)hd.n_pages,
+                                   cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    if (valid_lens && cudaMemcpyAsync(valid_lens, h->ws + h->g.L.page_valid, 4 * (size_t)hd.n_pages,
+                                      cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KVC_ERR_CUDA;
+  }
+  return KVC_OK;
+}
+
+int kvc_device_status(kvc_handle* h, kvc_stream stream) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (!h->device) return KVC_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t flag = 0;
+  if (cudaMemcpyAsync(&flag, h->ws + h->g.L.status, sizeof(flag), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (flag == 0) return KVC_OK;
+  if (cudaMemsetAsync(h->ws + h->g.L.status, 0, 256, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_ERR_DEVICE_TIMEOUT;
+}
+
+int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  switch (option) {
+    case KVC_OPT_ATTN_KERNEL:
+      if (value < 0 || value > 2) return KVC_ERR_INVALID_ARG;
+      if (value == 2 && !h->maps) return KVC_ERR_INVALID_ARG;
+      h->opt_kernel = (int)value;
+      h->has_plan = false;      // tile sizes differ between kernels
+      return KVC_OK;
+    case KVC_OPT_NUM_SPLITS:
+      if (value < 0 || value > h->cfg.max_kv_splits) return KVC_ERR_INVALID_ARG;
+      h->opt_splits = (int)value;
+      return KVC_OK;
+    case KVC_OPT_WAIT_BUDGET:
+      if (value < 0) return KVC_ERR_INVALID_ARG;
+      h->wait_budget = value;
+      return KVC_OK;
+    case KVC_OPT_TIMING:
+      if (value && !h->ev) {
+        if (!h->device) return KVC_ERR_NO_DEVICE;
+        cudaEvent_t* ev = (cudaEvent_t*)std::calloc(2 * kEventPairs, sizeof(cudaEvent_t));
+        bool* used = (bool*)std::calloc(kEventPairs, sizeof(bool));
+        if (!ev || !used) { std::free(ev); std::free(used); return KVC_ERR_INVALID_ARG; }
+        for (int i = 0; i < 2 * kEventPairs; ++i) {
+          if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+            std::free(ev);
+            std::free(used);
+            return KVC_ERR_CUDA;
+          }
+        }
+        h->ev = ev;
+        h->ev_used = used;
+      }
+      h->timing = value != 0;
+      return KVC_OK;
+    default:
+      return KVC_ERR_INVALID_ARG;
+  }
+}
+
+int kvc_get_counters(kvc_handle* h, int64_t* kernel_launches, int64_t* attn_launches, double* attn_ms,
+                     int32_t reset) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  drain_timing(h);
+  if (kernel_launches) *kernel_launches = h->launches;
+  if (attn_launches) *attn_launches = h->attn_launches;
+  if (attn_ms) *attn_ms = h->attn_ms;
+  if (reset) {
+    h->launches = 0;
+    h->attn_launches = 0;
+    h->attn_ms = 0.0;
+  }
+  return KVC_OK;
+}
+
+const char* kvc_strerror(int code) {
+  switch (code) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID_ARG: return "invalid argument";
+    case KVC_ERR_NO_FREE_PAGE: return "no free patch page";
+    case KVC_ERR_SPECIAL_POOL_FULL: return "special token pool full (max_total_frames reached)";
+    case KVC_ERR_NOTHING_TO_ROLLBACK: return "nothing to roll back";
+    case KVC_ERR_ROLLBACK_AFTER_EVICT: return "rollback after eviction";
+    case KVC_ERR_NO_PLAN: return "no plan";
+    case KVC_ERR_STALE_PLAN: return "stale plan: block state differs from the planned state";
+    case KVC_ERR_CUDA: return "CUDA error";
+    case KVC_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case KVC_ERR_EMPTY: return "no visible token";
+    case KVC_ERR_NO_DEVICE: return "bookkeeping-only handle";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

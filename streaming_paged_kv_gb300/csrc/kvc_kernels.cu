@@ -1,0 +1,295 @@
+// CUDA kernels of libkvc.so other than the tensor-core attention:
+//   append_kernel    -- scatter of one frame's K/V into its patch page and the
+//                       special stream (16-byte vector copies)
+//   plan_kernel      -- device page table, per-page valid lengths, KV tile list
+//   attn_simt_kernel -- paged attention on the CUDA cores (fp32 math), used for
+//                       fp32 caches and for head sizes without a tensor-core path
+//   merge_kernel     -- log-sum-exp merge of split-KV partial outputs
+//
+// Pages cited by tag, then section:
+//   [KVC]   "How LingBot-Map Implements the KV Cache Mechanism for Streaming
+//           Inference with FlashInfer Integration"
+//   [SLOTS] "LingBot-Map KV缓存机制深度揭秘：scale frames与keyframes如何占用slot"
+
+#include "kvc_internal.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace kvc {
+namespace {
+
+// ----------------------------------------------------------------- append
+// One frame's K/V [6 + ps, H, D]: rows 0..5 (camera, 4 registers, scale) go to
+// slots [special_slot, +6) of the special page, rows 6.. fill the patch page
+// ([SLOTS] "双流分页布局", "特殊 token 流"; [KVC] "Append and Evict API").
+// grid = (ceil(row16 / blockDim), 2 * (6 + ps)); one thread moves 16 bytes.
+__global__ void append_kernel(char* __restrict__ cache_block, const char* __restrict__ K,
+                              const char* __restrict__ V, int32_t page, int32_t special_page,
+                              int32_t special_slot, int32_t page_size, int64_t row_bytes) {
+  const int32_t T = kNumSpecial + page_size;
+  const int32_t kv = blockIdx.y / T;
+  const int32_t r = blockIdx.y - kv * T;
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c * 16 >= row_bytes) return;
+  const char* src = (kv ? V : K) + (int64_t)r * row_bytes + c * 16;
+  int64_t dst_row;
+  if (r < kNumSpecial)
+    dst_row = ((int64_t)special_page * 2 + kv) * page_size + special_slot + r;
+  else
+    dst_row = ((int64_t)page * 2 + kv) * page_size + (r - kNumSpecial);
+  uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+  *reinterpret_cast<uint4*>(cache_block + dst_row * row_bytes + c * 16) = v;
+}
+
+// ------------------------------------------------------------------- plan
+// Visible order: scale pages, live window, then every special page; a
+// non-last special page holds 6*fpp valid tokens, the last last_page_len
+// ([KVC] "Patch Pages vs. Special Pages"; [SLOTS] "双流分页布局").
+__global__ void plan_kernel(const __grid_constant__ PlanArgs a, char* __restrict__ ws,
+                            WorkspaceLayout L) {
+  const int32_t n_pages = a.n_patch + a.n_special;
+  const int32_t tr = a.tile_rows;
+  const int32_t tpp = (a.page_size + tr - 1) / tr;
+  const int32_t tps = (a.full_special_len + tr - 1) / tr;
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + L.page_ids);
+  int32_t* valid = reinterpret_cast<int32_t*>(ws + L.page_valid);
+  KvTile* tiles = reinterpret_cast<KvTile*>(ws + L.tiles);
+  for (int32_t i = threadIdx.x; i < n_pages; i += blockDim.x) {
+    const bool patch = i < a.n_patch;
+    const int32_t j = i - a.n_patch;
+    const int32_t id = patch ? a.patch_ids[i] : a.first_special + j;
+    const int32_t v = patch ? a.page_size : (i == n_pages - 1 ? a.last_page_len : a.full_special_len);
+    const int32_t tile0 = patch ? i * tpp : a.n_patch * tpp + j * tps;
+    const int32_t token0 = patch ? i * a.page_size : a.n_patch * a.page_size + j * a.full_special_len;
+    ids[i] = id;
+    valid[i] = v;
+    for (int32_t t = 0, r0 = 0; r0 < v; ++t, r0 += tr) {
+      KvTile k;
+      k.page = id;
+      k.row0 = r0;
+      k.rows = min(tr, v - r0);
+      k.token0 = token0 + r0;
+      tiles[tile0 + t] = k;
+    }
+  }
+  if (threadIdx.x == 0) {
+    DevPlanHeader h;
+    h.n_pages = n_pages;
+    h.last_page_len = a.last_page_len;
+    int32_t n_tiles = a.n_patch * tpp;
+    int32_t n_tokens = a.n_patch * a.page_size;
+    if (a.n_special > 0) {
+      n_tiles += (a.n_special - 1) * tps + (a.last_page_len + tr - 1) / tr;
+      n_tokens += (a.n_special - 1) * a.full_special_len + a.last_page_len;
+    }
+    h.n_tiles = n_tiles;
+    h.n_tokens = n_tokens;
+    *reinterpret_cast<DevPlanHeader*>(ws + L.header) = h;
+  }
+}
+
+// -------------------------------------------------------- element helpers
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <> __device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
+
+// ------------------------------------------------------ CUDA-core attention
+// One thread per query row, one CTA per (128-row query tile, head, KV split).
+// K/V tiles of BN rows are staged in shared memory as fp32; scores and the
+// online softmax are fp32, in the log2 domain (scores pre-multiplied by
+// sm_scale * log2 e).  Output: final O (one split) or the split's normalised
+// partial O and its log2-sum-exp.
+constexpr int kSimtThreads = 128;
+
+template <typename T, int D, int BN>
+__global__ void __launch_bounds__(kSimtThreads)
+attn_simt_kernel(const AttnArgs a) {
+  __shared__ float sK[BN][D];
+  __shared__ float sV[BN][D];
+  const int h = blockIdx.y;
+  const int split = blockIdx.z;
+  const int row = blockIdx.x * kSimtThreads + threadIdx.x;
+  const bool active = row < a.n_q;
+  const int H = a.num_heads;
+  const int64_t row_elems = (int64_t)H * D;
+  const T* qp = reinterpret_cast<const T*>(a.q) + ((int64_t)(active ? row : 0) * H + h) * D;
+  float q[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) q[d] = to_f(qp[d]) * a.sm_scale_log2;
+  float acc[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) acc[d] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  const int t0 = (int)(((int64_t)split * a.n_tiles) / a.n_splits);
+  const int t1 = (int)(((int64_t)(split + 1) * a.n_tiles) / a.n_splits);
+  const T* cache = reinterpret_cast<const T*>(a.cache);
+  for (int t = t0; t < t1; ++t) {
+    const KvTile tile = a.tiles[t];
+    const int64_t kbase = (((int64_t)tile.page * 2 + 0) * a.page_size + tile.row0) * row_elems + (int64_t)h * D;
+    const int64_t vbase = (((int64_t)tile.page * 2 + 1) * a.page_size + tile.row0) * row_elems + (int64_t)h * D;
+    for (int idx = threadIdx.x; idx < tile.rows * D; idx += kSimtThreads) {
+      const int r = idx / D, d = idx - r * D;
+      sK[r][d] = to_f(cache[kbase + (int64_t)r * row_elems + d]);
+      sV[r][d] = to_f(cache[vbase + (int64_t)r * row_elems + d]);
+    }
+    __syncthreads();
+    if (active) {
+      // Keys in chunks of 8: scores, chunk max, rescale, accumulate.
+      for (int j0 = 0; j0 < tile.rows; j0 += 8) {
+        float s[8];
+        float cmax = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          float x = -INFINITY;
+          if (j < tile.rows) {
+            x = 0.f;
+#pragma unroll
+            for (int d = 0; d < D; ++d) x = fmaf(q[d], sK[j][d], x);
+          }
+          s[jj] = x;
+          cmax = fmaxf(cmax, x);
+        }
+        const float m_new = fmaxf(m, cmax);
+        const float alpha = exp2f(m - m_new);
+        l *= alpha;
+#pragma unroll
+        for (int d = 0; d < D; ++d) acc[d] *= alpha;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          if (j < tile.rows) {
+            const float p = exp2f(s[jj] - m_new);
+            l += p;
+#pragma unroll
+            for (int d = 0; d < D; ++d) acc[d] = fmaf(p, sV[j][d], acc[d]);
+          }
+        }
+        m = m_new;
+      }
+    }
+    __syncthreads();
+  }
+  if (!active) return;
+  const float inv = 1.f / l;
+  if (a.n_splits == 1) {
+    T* op = reinterpret_cast<T*>(a.out) + ((int64_t)row * H + h) * D;
+#pragma unroll
+    for (int d = 0; d < D; ++d) op[d] = from_f<T>(acc[d] * inv);
+  } else {
+    float* po = a.part_o + (((int64_t)split * a.n_q + row) * H + h) * D;
+#pragma unroll
+    for (int d = 0; d < D; ++d) po[d] = acc[d] * inv;
+    a.part_lse[((int64_t)split * a.n_q + row) * H + h] = m + log2f(l);
+  }
+}
+
+// -------------------------------------------------------------- LSE merge
+// out = sum_s 2^(lse_s - lse) O_s with lse = log2 sum_s 2^lse_s; one warp per
+// (query row, head).
+template <typename T, int D>
+__global__ void merge_kernel(const AttnArgs a) {
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = a.num_heads;
+  if (w >= (int64_t)a.n_q * H) return;
+  const int64_t row = w / H;
+  const int h = (int)(w - row * H);
+  float mx = -INFINITY;
+  for (int s = 0; s < a.n_splits; ++s) mx = fmaxf(mx, a.part_lse[((int64_t)s * a.n_q + row) * H + h]);
+  float wsum = 0.f;
+  float o[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) o[i] = 0.f;
+  for (int s = 0; s < a.n_splits; ++s) {
+    const float wt = exp2f(a.part_lse[((int64_t)s * a.n_q + row) * H + h] - mx);
+    wsum += wt;
+    const float* po = a.part_o + (((int64_t)s * a.n_q + row) * H + h) * D;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) o[i] = fmaf(wt, po[lane + 32 * i], o[i]);
+  }
+  const float inv = 1.f / wsum;
+  T* op = reinterpret_cast<T*>(a.out) + (row * H + h) * D;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) op[lane + 32 * i] = from_f<T>(o[i] * inv);
+}
+
+template <typename T, int D>
+cudaError_t simt_dispatch(const AttnArgs& a, cudaStream_t st) {
+  constexpr int BN = D >= 128 ? 32 : 64;
+  dim3 grid((a.n_q + kSimtThreads - 1) / kSimtThreads, a.num_heads, a.n_splits);
+  attn_simt_kernel<T, D, BN><<<grid, kSimtThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t simt_by_dim(const AttnArgs& a, cudaStream_t st) {
+  switch (a.head_dim) {
+    case 32: return simt_dispatch<T, 32>(a, st);
+    case 64: return simt_dispatch<T, 64>(a, st);
+    case 128: return simt_dispatch<T, 128>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t merge_by_dim(const AttnArgs& a, cudaStream_t st) {
+  const int64_t warps = (int64_t)a.n_q * a.num_heads;
+  const int threads = 256;
+  const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
+  switch (a.head_dim) {
+    case 32: merge_kernel<T, 32><<<blocks, threads, 0, st>>>(a); break;
+    case 64: merge_kernel<T, 64><<<blocks, threads, 0, st>>>(a); break;
+    case 128: merge_kernel<T, 128><<<blocks, threads, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int simt_tile_rows(int head_dim) { return head_dim >= 128 ? 32 : 64; }
+
+cudaError_t launch_append(void* cache_block, const void* K, const void* V, int32_t page,
+                          int32_t special_page, int32_t special_slot, int32_t page_size,
+                          int64_t row_bytes, cudaStream_t stream) {
+  const int64_t row16 = row_bytes / 16;
+  const int threads = row16 >= 128 ? 128 : (int)((row16 + 31) / 32 * 32);
+  dim3 grid((unsigned)((row16 + threads - 1) / threads), 2u * (unsigned)(kNumSpecial + page_size));
+  append_kernel<<<grid, threads, 0, stream>>>(static_cast<char*>(cache_block),
+                                             static_cast<const char*>(K), static_cast<const char*>(V),
+                                             page, special_page, special_slot, page_size, row_bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const PlanArgs& a, void* workspace, const WorkspaceLayout& L,
+                        cudaStream_t stream) {
+  plan_kernel<<<1, 256, 0, stream>>>(a, static_cast<char*>(workspace), L);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_simt(const AttnArgs& a, int dtype, cudaStream_t stream) {
+  switch (dtype) {
+    case 0: return simt_by_dim<__nv_bfloat16>(a, stream);
+    case 1: return simt_by_dim<__half>(a, stream);
+    case 2: return simt_by_dim<float>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_merge(const AttnArgs& a, int dtype, cudaStream_t stream) {
+  switch (dtype) {
+    case 0: return merge_by_dim<__nv_bfloat16>(a, stream);
+    case 1: return merge_by_dim<__half>(a, stream);
+    case 2: return merge_by_dim<float>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvc

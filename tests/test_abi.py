@@ -1,0 +1,56 @@
+"""The C-ABI library loads on a machine without a GPU and exports every
+function include/kvc.h declares; configuration validation needs no GPU."""
+
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    from streaming_paged_kv_gb300 import build
+    build.build()
+    from streaming_paged_kv_gb300 import kvc as mod
+    return mod
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kvc.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(kvc):
+    names = declared_functions()
+    assert len(names) >= 19
+    missing = [n for n in names if not hasattr(kvc.lib, n)]
+    assert not missing, missing
+
+
+def test_required_bytes_and_validation(kvc):
+    cfg = kvc.make_config(24, 16, 64, 999)
+    cache, ws = kvc.kvc_required_bytes(cfg)
+    # 88 patch + ceil(2048/166) = 13 special pages, K and V, 999 rows of 16*64 bf16 per block.
+    assert cache == 24 * 101 * 2 * 999 * 16 * 64 * 2
+    assert ws > 0
+    for bad in (dict(head_dim=48), dict(page_size=5), dict(num_heads=0),
+                dict(scale_frames=2000), dict(max_kv_splits=1000)):
+        args = dict(num_blocks=1, num_heads=16, head_dim=64, page_size=256)
+        args.update(bad)
+        with pytest.raises(kvc.KvcError) as e:
+            kvc.kvc_required_bytes(kvc.make_config(**args))
+        assert e.value.code == "INVALID_ARG"
+
+
+def test_bookkeeping_handle_refuses_device_calls(kvc):
+    c = kvc.PagedKVCache(1, 2, 32, 16, "f32", 2, 4, 2, 16, device=None)
+    c.append_frame(0)
+    c.plan()
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.kvc_run(c.h, 0, None, None, 0)
+    assert e.value.code == "NO_DEVICE"
+    assert kvc.kvc_device_status(c.h) == -11
+    assert kvc.kvc_strerror(-7).startswith("stale plan")
