@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Streamed frames/s of the 24-layer 518x378 exact-page paged-attention stream.
+
+A step is one streamed frame through every block: per block append_frame,
+evict_frames, (plan on block 0) and the paged attention run, all through the
+C ABI of libkvc.so.  The stream is the 518x378 workload (page_size 999, H=16,
+D=64, bf16, 8 scale / 64 window / 16 headroom pages, 2048 frames).  The timed
+steps are the LAST K frames of that 2048-frame stream: the frames before them
+are streamed untimed (append + evict only, then W full warm-up frames), so the
+number always describes the same part of the stream whatever K is; the
+default K covers the whole stream after the warm-up.
+
+Inputs are synthetic: a pool of seeded N(0,1) bf16 Q/K/V frames per layer,
+resident in HBM before the timed region (K scaled per head by a seeded
+U(0.5, 2) factor); frame f of layer b uses pool entry (f + b) mod pool.  Every
+layer's visible K/V (~340 MB at full context) is larger than L2, so no flush is
+needed between steps.
+
+Output: one JSON line (see the keys below).  ``--impl reference`` times the CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "streamed frames/s (24-layer paged attn, 518x378); attn TFLOP/s vs GB300 roofline"
+UNIT = "frames/s"
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None, help="timed frames (default: rest of the stream)")
+    p.add_argument("--warmup", type=int, default=16)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="s518")
+    p.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
+    p.add_argument("--pool", type=int, default=4, help="distinct input frames per layer")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=64)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        for line in open(self.file.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------- GPU stream
+class Stream:
+    """One device stream of the workload through the library."""
+
+    def __init__(self, kvc, w, pool, seed, kernel, dev):
+        import torch
+        from streaming_paged_kv_gb300.inputs import k_head_scale
+        self.torch, self.kvc, self.w = torch, kvc, w
+        self.c = kvc.PagedKVCache(w.num_layers, w.num_heads, w.head_dim, w.page_size, w.dtype,
+                                  w.scale_frames, w.sliding_window, w.headroom, w.max_total_frames,
+                                  device=dev)
+        if kernel:
+            self.c.set_option(kvc.KVC_OPT_ATTN_KERNEL, kernel)
+        T, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        scale = torch.from_numpy(k_head_scale(seed, w.wid, H)).to(dev) if w.k_head_scale else None
+        self.pool = []
+        for i in range(pool):
+            per_layer = []
+            for b in range(w.num_layers):
+                q = torch.randn(T, H, D, generator=g, device=dev).to(torch.bfloat16)
+                k = torch.randn(T, H, D, generator=g, device=dev)
+                if scale is not None:
+                    k = k * scale[None, :, None]
+                k = k.to(torch.bfloat16)
+                v = torch.randn(T, H, D, generator=g, device=dev).to(torch.bfloat16)
+                per_layer.append((q, k, v))
+            self.pool.append(per_layer)
+        self.out = [torch.empty(T, H, D, dtype=torch.bfloat16, device=dev) for _ in range(w.num_layers)]
+        self.frame = 0
+
+    def inputs(self, f, b):
+        return self.pool[(f + b) % len(self.pool)][b]
+
+    def fast_forward(self, n):
+        """Append + evict only (no attention) for n frames."""
+        c = self.c
+        for _ in range(n):
+            for b in range(self.w.num_layers):
+                _, k, v = self.inputs(self.frame, b)
+                c.append_frame(b, k, v)
+                c.evict_frames(b)
+            self.frame += 1
+
+    def step(self):
+        """One streamed frame: append, evict, plan (block 0), attention per block."""
+        c = self.c
+        for b in range(self.w.num_layers):
+            q, k, v = self.inputs(self.frame, b)
+            c.append_frame(b, k, v)
+            c.evict_frames(b)
+            if b == 0:
+                c.plan()
+            c.run(b, q, self.out[b])
+        self.frame += 1
+
+    def visible_tokens(self):
+        s = self.c.stats(0)
+        return self.w.page_size * (s["scale_pages"] + s["live_pages"]) + s["special_tokens"]
+
+
+def run_ours(args, rank, world):
+    import torch
+    from streaming_paged_kv_gb300 import build
+    build.build()
+    from streaming_paged_kv_gb300 import kvc
+    from streaming_paged_kv_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    K = args.steps if args.steps is not None else w.n_frames - args.warmup
+    W = args.warmup
+    K = max(1, min(K, w.n_frames))
+    W = max(0, min(W, w.n_frames - K))
+    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev)
+    st.fast_forward(w.n_frames - K - W)
+    for _ in range(W):
+        st.step()
+    torch.cuda.synchronize()
+    # Algorithmic work of the timed frames (attention only): replay the same
+    # frames on a bookkeeping-only handle to get each frame's visible tokens.
+    n_q, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
+    book = kvc.PagedKVCache(1, H, D, w.page_size, w.dtype, w.scale_frames, w.sliding_window,
+                            w.headroom, w.max_total_frames, device=None)
+    flops = bytes_alg = 0.0
+    for f in range(w.n_frames):
+        book.append_frame(0)
+        book.evict_frames(0)
+        if f >= w.n_frames - K:
+            s = book.stats(0)
+            nkv = w.page_size * (s["scale_pages"] + s["live_pages"]) + s["special_tokens"]
+            flops += w.num_layers * 4.0 * n_q * nkv * H * D
+            bytes_alg += w.num_layers * (2.0 * nkv * H * D * 2 + 2.0 * n_q * H * D * 2)
+    book.close()
+    kvc.kvc_get_counters(st.c.h, reset=True)
+    st.c.set_option(kvc.KVC_OPT_TIMING, 1)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    ev0.record()
+    for _ in range(K):
+        st.step()
+    ev1.record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    launches, attn_launches, attn_ms = kvc.kvc_get_counters(st.c.h, reset=True)
+    st.c.set_option(kvc.KVC_OPT_TIMING, 0)
+    status = kvc.kvc_device_status(st.c.h, st.c._stream())
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    value = world * K / (ms / 1e3)
+    pk = peaks()
+    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
+    roofline = {
+        "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
+        "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None,
+        "traffic": None,
+        "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
+        "kernel": "paged attention (kvc_run attention launch)",
+        "flops_per_launch": flops / max(attn_launches, 1),
+        "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
+        "launch_ms": attn_ms / max(attn_launches, 1),
+        "hbm_frac_alg": (bytes_alg / (attn_ms / 1e3) / 1e9) / pk["hbm_gbs"] if attn_ms > 0 else None,
+    }
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: 518x378 exact-page stream, {w.num_layers} layers, "
+                               f"H={H}, D={D}, page_size={w.page_size}, {w.n_frames} frames; timed = "
+                               f"last {K} frames",
+                   "frames_timed": [w.n_frames - K, w.n_frames - 1],
+                   "l2": "no flush: every layer's visible K/V (>300 MB at full context) exceeds L2",
+                   "parallelism": f"replicas x{world} (independent streams, no collective)",
+                   "wall_s": t_wall},
+        "roofline": roofline,
+        "attn_tflops": achieved,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    del st
+    torch.cuda.empty_cache()
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, kvc, w, dev, rank, world)
+    return res
+
+
+def run_e2e(args, kvc, w, dev, rank, world):
+    """The same frames/s through the public API with host inputs: every step
+    copies that frame's Q/K/V of every layer from pinned host memory and reads
+    every layer's output back to pinned host memory inside the timed region."""
+    import torch
+    K = max(1, min(args.e2e_steps, w.n_frames))
+    W = min(4, w.n_frames - K)
+    T, H, D, L = w.tokens_per_frame, w.num_heads, w.head_dim, w.num_layers
+    c = kvc.PagedKVCache(L, H, D, w.page_size, w.dtype, w.scale_frames, w.sliding_window,
+                         w.headroom, w.max_total_frames, device=dev)
+    g = torch.Generator()
+    g.manual_seed(args.seed + 1000 + rank)
+    host = [[torch.randn(T, H, D, generator=g).to(torch.bfloat16).pin_memory() for _ in range(3)]
+            for _ in range(L)]
+    host_out = [torch.empty(T, H, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    dq = [torch.empty(T, H, D, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    dout = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+
+    def frame(attend=True):
+        for b in range(L):
+            for i in range(3):
+                dq[i].copy_(host[b][i], non_blocking=True)
+            c.append_frame(b, dq[1], dq[2])
+            c.evict_frames(b)
+            if not attend:
+                continue
+            if b == 0:
+                c.plan()
+            c.run(b, dq[0], dout)
+            host_out[b].copy_(dout, non_blocking=True)
+
+    for _ in range(w.n_frames - K - W):
+        frame(attend=False)
+    for _ in range(W):
+        frame()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        frame()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    c.close()
+    return {"value": world * K / dt, "unit": UNIT, "h2d_bytes_per_step": L * 3 * T * H * D * 2,
+            "d2h_bytes_per_step": L * T * H * D * 2, "steps": K,
+            "frames_timed": [w.n_frames - K, w.n_frames - 1]}
+
+
+# ------------------------------------------------------------- CPU oracle
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+class OracleStream:
+    """The oracle at the end of the stream: bookkeeping of every frame and the
+    cache mirror of one block, filled by appending one fixed frame repeatedly
+    (values do not change the oracle's cost)."""
+
+    def __init__(self, w, seed):
+        import numpy as np
+        from oracle import OraclePagedKV
+        from streaming_paged_kv_gb300.inputs import frame_qkv, k_head_scale, to_bits
+        self.np = np
+        self.w = w
+        hs = k_head_scale(seed, w.wid, w.num_heads) if w.k_head_scale else None
+        q, k, v = frame_qkv(seed, w.wid, 0, 0, w.page_size, w.num_heads, w.head_dim, w.dtype, hs)
+        self.q, self.k, self.v = to_bits(q), to_bits(k), to_bits(v)
+        self.orc = OraclePagedKV(1, w.page_size, w.num_heads, w.head_dim, w.dtype, w.scale_frames,
+                                 w.sliding_window, w.headroom, w.max_total_frames, mirror_blocks=(0,))
+        for _ in range(w.n_frames):
+            self.orc.append_frame(0, self.k, self.v)
+            self.orc.evict_frames(0, w.scale_frames, w.sliding_window)
+
+    def attention_seconds(self, rows):
+        from oracle import paged_attention
+        t0 = time.perf_counter()
+        paged_attention(self.orc, 0, self.q, rows=rows)
+        return time.perf_counter() - t0
+
+    def bookkeeping_seconds_per_frame(self, n=64):
+        import numpy as np
+        from oracle import OraclePagedKV
+        w = self.w
+        o = OraclePagedKV(w.num_layers, w.page_size, w.num_heads, w.head_dim, w.dtype,
+                          w.scale_frames, w.sliding_window, w.headroom, w.max_total_frames,
+                          mirror_blocks=())
+        t0 = time.perf_counter()
+        for _ in range(n):
+            for b in range(w.num_layers):
+                o.append_frame(b, self.k, self.v)
+                o.evict_frames(b, w.scale_frames, w.sliding_window)
+            o.visible_page_table(0)
+        return (time.perf_counter() - t0) / n
+
+
+def cpu_baseline(w, seed, budget_s):
+    """Oracle frames/s at the end of the stream, from a bounded row sample of
+    one layer's attention, extrapolated to all rows and all layers."""
+    os_ = OracleStream(w, seed)
+    n_q = w.tokens_per_frame
+    rows_done, secs = 0, 0.0
+    chunk = 16
+    while secs < budget_s and rows_done < n_q:
+        rows = list(range(rows_done, min(n_q, rows_done + chunk)))
+        secs += os_.attention_seconds(rows)
+        rows_done += len(rows)
+        chunk = min(chunk * 2, 128)
+    per_layer = secs * n_q / rows_done
+    book = os_.bookkeeping_seconds_per_frame(8)
+    per_frame = per_layer * w.num_layers + book
+    return {"value": 1.0 / per_frame, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"last frame of the {w.n_frames}-frame stream "
+                      f"({sum(os_.orc.visible_page_table(0)[3])} visible tokens): "
+                      f"{rows_done}/{n_q} query rows x {w.num_heads} heads of one layer in {secs:.1f} s, "
+                      f"scaled to {n_q} rows x {w.num_layers} layers, plus "
+                      f"{book * 1e3:.2f} ms bookkeeping per frame"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded sample of a
+    frame at the end of the stream (a slice of one layer's query rows),
+    extrapolated to a whole frame."""
+    from streaming_paged_kv_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    K = args.steps if args.steps is not None else 8
+    W = args.warmup if args.warmup is not None else 3
+    K, W = max(1, K), max(0, W)
+    os_ = OracleStream(w, args.seed)
+    n_q = w.tokens_per_frame
+    t1 = os_.attention_seconds(list(range(8))) / 8          # calibration: seconds per row
+    total_budget = 90.0
+    rows = int(max(1, min(n_q, total_budget / max(K + W, 1) / max(t1, 1e-6))))
+    sel = list(range(rows))
+    for _ in range(W):
+        os_.attention_seconds(sel)
+    book = os_.bookkeeping_seconds_per_frame(4)
+    secs = 0.0
+    for _ in range(K):
+        secs += os_.attention_seconds(sel)
+    per_frame = secs / K * n_q / rows * w.num_layers + book
+    value = 1.0 / per_frame
+    cb = {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+          "sample": f"per step: {rows}/{n_q} query rows x {w.num_heads} heads of one layer of the last "
+                    f"frame, scaled to a {w.num_layers}-layer frame, plus bookkeeping"}
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": K, "warmup": W, "ms_per_step": per_frame * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: 518x378 exact-page stream, {w.num_layers} layers, "
+                                   f"H={w.num_heads}, D={w.head_dim}, page_size={w.page_size}, "
+                                   f"{w.n_frames} frames; oracle on a row sample of the last frame"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        from streaming_paged_kv_gb300.workloads import WORKLOADS
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(WORKLOADS[args.workload], args.seed, args.cpu_budget)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
