@@ -58,7 +58,8 @@ enum {
   KVC_ERR_CUDA = -8,                /* a CUDA runtime call failed                    */
   KVC_ERR_DEVICE_TIMEOUT = -9,      /* a kernel gave up waiting (kvc_device_status)  */
   KVC_ERR_EMPTY = -10,              /* plan of a cache with no visible token         */
-  KVC_ERR_NO_DEVICE = -11           /* device call on a bookkeeping-only handle      */
+  KVC_ERR_NO_DEVICE = -11,          /* device call on a bookkeeping-only handle      */
+  KVC_ERR_TOO_LARGE = -12           /* beyond kvc_paged_attention_static's scratch   */
 };
 
 typedef struct kvc_handle kvc_handle;
@@ -207,6 +208,31 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
  * milliseconds (synchronises the pending timing events). */
 int kvc_get_counters(kvc_handle* h, int64_t* kernel_launches, int64_t* attn_launches,
                      double* attn_ms, int32_t reset);
+
+/* Paged attention that allocates nothing.  The pages have no counterpart to
+ * this call; it exists for callers that cannot allocate device memory -- for
+ * example code embedded in a host framework that owns all GPU memory and lends
+ * out only the KV cache and the Q / output buffers, so that it cannot provide
+ * the workspace kvc_create needs.  It computes what kvc_run computes (CUDA-core
+ * kernel, split-KV partials merged by log-sum-exp) for one block's cache, but
+ * keeps all its scratch (KV tile list, partial outputs, status word) in a
+ * 32 MiB array inside the library, which every GPU that runs it holds until
+ * the process exits.  It calls no cudaMalloc / cudaFree.
+ *   cache_block: device [pages][2][page_size][H][D] of `dtype` (one block).
+ *   page_ids, valid_lens: HOST arrays of n_pages entries, in attention order;
+ *     each id must address a page of cache_block, 1 <= valid_lens[i] <=
+ *     page_size.  Q, out: device [n_q, H, D].  sm_scale 0 => 1/sqrt(D).
+ * Limits: n_pages <= 1024 and at most 16384 KV tiles (64 rows each, 32 for
+ * head_dim 128), else KVC_ERR_TOO_LARGE; the number of KV splits is cut to
+ * what fits in the array.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Every call shares the one array, so
+ * calls whose work overlaps on the GPU (other streams, other threads) race:
+ * serialise them.  The status word is cleared on every call. */
+int kvc_paged_attention_static(const void* cache_block, int32_t dtype, int32_t num_heads,
+                               int32_t head_dim, int32_t page_size, const int32_t* page_ids,
+                               const int32_t* valid_lens, int32_t n_pages, const void* Q, void* out,
+                               int32_t n_q, float sm_scale, kvc_stream stream);
 
 /* Static message for a status code. */
 const char* kvc_strerror(int code);

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkvc.so")
 STAMP = os.path.join(PKG, "libkvc.machine")
-SOURCES = ["kvc_host.cpp", "kvc_kernels.cu", "kvc_attn_tc.cu"]
+SOURCES = ["kvc_host.cpp", "kvc_kernels.cu", "kvc_attn_tc.cu", "kvc_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

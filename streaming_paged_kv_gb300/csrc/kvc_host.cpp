@@ -672,6 +672,7 @@ const char* kvc_strerror(int code) {
     case KVC_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case KVC_ERR_EMPTY: return "no visible token";
     case KVC_ERR_NO_DEVICE: return "bookkeeping-only handle";
+    case KVC_ERR_TOO_LARGE: return "too many pages or KV tiles for the static scratch array";
     default: return "unknown error";
   }
 }

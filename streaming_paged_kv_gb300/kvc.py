@@ -25,7 +25,7 @@ DTYPE_CODE = {"bf16": KVC_BF16, "f16": KVC_F16, "f32": KVC_F32}
 ERRORS = {
     0: "OK", -1: "INVALID_ARG", -2: "NO_FREE_PAGE", -3: "SPECIAL_POOL_FULL",
     -4: "NOTHING_TO_ROLLBACK", -5: "ROLLBACK_AFTER_EVICT", -6: "NO_PLAN", -7: "STALE_PLAN",
-    -8: "CUDA", -9: "DEVICE_TIMEOUT", -10: "EMPTY", -11: "NO_DEVICE",
+    -8: "CUDA", -9: "DEVICE_TIMEOUT", -10: "EMPTY", -11: "NO_DEVICE", -12: "TOO_LARGE",
 }
 KVC_OPT_ATTN_KERNEL, KVC_OPT_NUM_SPLITS, KVC_OPT_WAIT_BUDGET, KVC_OPT_TIMING = 1, 2, 3, 4
 
@@ -80,6 +80,8 @@ _SIGS = {
     "kvc_set_option": [_P, _I32, _I64],
     "kvc_get_counters": [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                          ctypes.POINTER(ctypes.c_double), _I32],
+    "kvc_paged_attention_static": [_P, _I32, _I32, _I32, _I32, _PI32, _PI32, _I32, _P, _P, _I32,
+                                   ctypes.c_float, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -201,6 +203,20 @@ def kvc_get_counters(h, reset=False):
     _check(lib.kvc_get_counters(h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(ms), int(reset)),
            "kvc_get_counters")
     return a.value, b.value, ms.value
+
+
+def kvc_paged_attention_static(cache_ptr, dtype, num_heads, head_dim, page_size, page_ids,
+                               valid_lens, q_ptr, out_ptr, n_q, sm_scale=0.0, stream=None):
+    """Paged attention with no allocation (scratch inside the library): for
+    callers that cannot allocate device memory.  page_ids / valid_lens are
+    host sequences; see include/kvc.h for the limits and the sharing rules."""
+    n = len(page_ids)
+    ids = (ctypes.c_int32 * max(n, 1))(*page_ids)
+    valid = (ctypes.c_int32 * max(n, 1))(*valid_lens)
+    return _check(lib.kvc_paged_attention_static(cache_ptr, DTYPE_CODE.get(dtype, dtype), num_heads,
+                                                 head_dim, page_size, ids, valid, n, q_ptr, out_ptr,
+                                                 n_q, float(sm_scale), stream),
+                  "kvc_paged_attention_static")
 
 
 def kvc_strerror(rc):
