@@ -1,15 +1,614 @@
-// Tensor-core (tcgen05) paged attention -- not yet enabled.
+// Tensor-core paged attention for sm_103a: TMA gathers of K/V page tiles
+// through the page table, tcgen05 MMAs with TMEM accumulators, fp32 online
+// softmax.
+//
+// What it computes ([KVC] "Kernel-Level Execution Flow": causal=False,
+// pos_encoding_mode="NONE", as many KV heads as query heads):
+//     O[t,h,:] = sum_j softmax_j(Q[t,h,:].K[j,h,:] * sm_scale) V[j,h,:]
+// over the visible tokens j, which the plan lists as KV tiles of at most 128
+// rows of one page (scale pages, live window, then the special pages; a
+// page's rows beyond its valid count never enter the softmax, so exact page
+// sizes such as 999 need no padding -- [PERF] "Page-Size Handling for FA2 vs
+// FA3").
+//
+// Pages cited by tag: [KVC] "How LingBot-Map Implements the KV Cache Mechanism
+// for Streaming Inference with FlashInfer Integration"; [PERF] "How to Improve
+// Streaming Inference Performance with FlashInfer KV Cache Backend".
+//
+// CTA = one 128-row query tile x one head x one KV split.  Warps:
+//   0-3  softmax + epilogue: thread r owns query row r (TMEM lane r)
+//   4    TMA producer (one lane): Q once, then K/V tiles into a 3-stage ring
+//   5    MMA issuer (one lane): S = Q K^T into TMEM (double-buffered),
+//        O += P V into TMEM
+// Shared memory tiles use the 128-byte swizzle that both TMA and the tensor
+// core understand; P (bf16/f16) is written by the softmax threads into the
+// same swizzled K-major layout.  Scores live in the log2 domain (scaled by
+// sm_scale * log2 e).  O is rescaled lazily: only when a row's running max
+// grows by more than 8 (a factor 256), otherwise P is taken against the stale
+// max, which fp32 accumulation absorbs.
+//
+// Every mbarrier wait is bounded: when a wait runs out, the thread records
+// the fact in the status word, raises a CTA-wide abort flag, and every role
+// skips its remaining work, drains its own in-flight copies / MMAs (again
+// with a bound), frees TMEM and returns.
+
 #include "kvc_internal.h"
 
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdlib>
+#include <new>
+#include <type_traits>
+
 namespace kvc {
-struct TcMaps {};
-bool tc_supported(int, int, int, int) { return false; }
-TcMaps* tc_create_maps(void*, int, int, int, int, int, int, cudaError_t* err) {
-  if (err) *err = cudaErrorNotSupported;
-  return nullptr;
+
+struct TcMaps {
+  CUtensorMap cache;     // 3D view of the whole cache: {H*D, page_size, blocks*pages*2}
+  int dtype;
+  int num_heads;
+  int head_dim;
+};
+
+namespace {
+
+constexpr int BM = 128;           // query rows per CTA
+constexpr int BN = 128;           // KV rows per tile
+constexpr int HD = 64;            // head dim of this kernel
+constexpr int STAGES = 3;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TILE_BYTES = BN * HD * 2;         // 16 KB: one K or V tile
+constexpr uint32_t Q_BYTES = BM * HD * 2;            // 16 KB
+constexpr uint32_t P_BYTES = BM * BN * 2;            // 32 KB: two 64-column chunks
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL0 = 0, O_COL = 256;
+constexpr float RESCALE_THRESHOLD = 8.0f;            // log2 units
+constexpr long long kDrainBudget = 1LL << 26;        // cycles for draining after an abort
+
+// Shared memory map (offsets from a 1024-aligned base).
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
+constexpr uint32_t OFF_P = OFF_V + STAGES * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+
+// ------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-void tc_destroy_maps(TcMaps*) {}
-cudaError_t launch_attn_tc(const AttnArgs&, TcMaps*, int, int, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait.  Returns false when the CTA is (or becomes) aborted.
+struct Guard {
+  volatile int* abort_flag;   // shared
+  int32_t* status;            // global
+  long long budget;
+};
+
+__device__ __noinline__ void raise_abort(const Guard& g, int where) {
+  *g.abort_flag = 1;
+  if (atomicCAS(g.status, 0, 1) == 0) {
+    g.status[1] = where;
+    g.status[2] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  }
+  __threadfence();
+}
+
+__device__ __forceinline__ bool wait_bar(const Guard& g, uint64_t* bar, uint32_t parity, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (*g.abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > g.budget) {
+      raise_abort(g, where);
+      return false;
+    }
+  }
+}
+
+// Bounded wait whose outcome is the same for all 32 lanes of the warp (the
+// warp-collective tcgen05.ld / st that follow need a converged warp).
+__device__ __forceinline__ bool wait_bar_warp(const Guard& g, uint64_t* bar, uint32_t parity, int where) {
+  const bool ok = wait_bar(g, bar, parity, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Wait with a fixed budget, ignoring the abort flag (used to drain).
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kDrainBudget) {
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
+// start>>4 in [0,14), LBO>>4 in [16,30), SBO>>4 in [32,46), version 1 at 46,
+// swizzle mode 2 = 128B at [61,64)).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation: A and B both
+// bf16 (or both f16), A K-major, B K-major or MN-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+        "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+        "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
+      "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
+      "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Ties the registers to a point after tcgen05.wait::ld so that no use of them
+// is scheduled before the wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[i])::"memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&t);
+  } else {
+    __half2 t = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&t);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_row(void* dst, const float* o, float inv) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i) {
+    uint4 u;
+    u.x = pack2<BF16>(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
+    u.y = pack2<BF16>(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
+    u.z = pack2<BF16>(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
+    u.w = pack2<BF16>(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
+    d[i] = u;
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
+               const __grid_constant__ CUtensorMap q_map, int32_t page_base) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + OFF_Q;
+  uint8_t* sK = smem + OFF_K;
+  uint8_t* sV = smem + OFF_V;
+  uint8_t* sP = smem + OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;                 // [STAGES]
+  uint64_t* kv_empty = bars + 1 + STAGES;       // [STAGES]
+  uint64_t* s_full = bars + 1 + 2 * STAGES;     // [2]
+  uint64_t* p_full = bars + 3 + 2 * STAGES;     // [2]
+  uint64_t* p_free = bars + 5 + 2 * STAGES;     // [2]
+  uint64_t* drain = bars + 7 + 2 * STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * STAGES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
+  const int q0 = qt * BM;
+  const int t0 = (int)(((int64_t)split * a.n_tiles) / a.n_splits);
+  const int t1 = (int)(((int64_t)(split + 1) * a.n_tiles) / a.n_splits);
+  const int n = t1 - t0;
+  Guard g{abort_flag, a.status, a.wait_budget};
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], BM);
+      mbar_init(&p_free[b], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0 && n > 0) {
+      int issued = 0;
+      mbar_expect_tx(q_full, Q_BYTES);
+      tma_load_2d(sQ, &q_map, h * HD, q0, q_full);
+      for (int j = 0; j < n; ++j) {
+        const int st = j % STAGES;
+        if (j >= STAGES && !wait_bar(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
+        const KvTile tile = a.tiles[t0 + j];
+        const int plane = (page_base + tile.page) * 2;
+        mbar_expect_tx(&kv_full[st], 2 * TILE_BYTES);
+        tma_load_3d(sK + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane, &kv_full[st]);
+        tma_load_3d(sV + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // Let every copy this thread started land before the CTA exits.
+        drain_bar(q_full, 0);
+        for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
+          drain_bar(&kv_full[j % STAGES], (j / STAGES) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(BM, BN, BF16, false);
+      constexpr uint32_t IDESC_O = idesc_f16(BM, HD, BF16, true);
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+      bool ok = wait_bar(g, q_full, 0, 2);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % STAGES;
+        if (!wait_bar(g, &kv_full[st], (j / STAGES) & 1, 3)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + S_COL0 + (j & 1) * BN;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k)
+          umma(d, sdesc_sw128(aQ + k * 32, 16, 1024), sdesc_sw128(aK + st * TILE_BYTES + k * 32, 16, 1024),
+               IDESC_S, k > 0);
+        umma_commit(&s_full[j & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n && !issue_s(j + 1)) break;
+        const int b = j & 1, st = j % STAGES;
+        if (!wait_bar(g, &p_full[b], (j >> 1) & 1, 4)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t a_addr = aP + b * P_BYTES + (k >> 2) * (BM * 128) + (k & 3) * 32;
+          const uint32_t b_addr = aV + st * TILE_BYTES + k * 16 * 128;
+          umma(tmem + O_COL, sdesc_sw128(a_addr, 16, 1024), sdesc_sw128(b_addr, BN * 128, 1024), IDESC_O,
+               (j > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(&kv_empty[st]);
+        umma_commit(&p_free[b]);
+      }
+      // Every MMA this thread issued has completed once `drain` flips.
+      umma_commit(drain);
+      drain_bar(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------ softmax + epilogue
+    const int r = threadIdx.x;                       // query row within the tile == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = a.sm_scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = n > 0;
+    uint8_t* prow = sP + r * 128;
+    const int sw = r & 7;
+    for (int j = 0; ok && j < n; ++j) {
+      const int b = j & 1;
+      const int rows_valid = a.tiles[t0 + j].rows;
+      if (!wait_bar_warp(g, &s_full[b], (j >> 1) & 1, 5)) { ok = false; break; }
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + S_COL0 + b * BN + c * 32, v);
+        tmem_wait_ld();
+        reg_fence(v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, c < rows_valid ? s[c] : -INFINITY);
+      const float m_tile = mx * sl2;
+      const bool need = m_tile > m_ref + RESCALE_THRESHOLD;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? fmaxf(m_ref, m_tile) : m_ref;
+        const float alpha = ex2(m_ref - m_new);      // 0 on the first tile
+        if (j > 0) {
+          // The previous P V product must have landed before O is rescaled.
+          if (!wait_bar_warp(g, &p_free[b ^ 1], ((j - 1) >> 1) & 1, 6)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + O_COL + c * 32, v);
+            tmem_wait_ld();
+            reg_fence(v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(lane_base + O_COL + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      // P buffer b is free once the P V product of tile j-2 has completed.
+      if (j >= 2 && !wait_bar_warp(g, &p_free[b], ((j - 2) >> 1) & 1, 7)) { ok = false; break; }
+      const float neg = -m_ref;
+      uint8_t* pb = prow + b * P_BYTES;
+#pragma unroll
+      for (int c16 = 0; c16 < BN / 8; ++c16) {       // 16 chunks of 8 columns (16 bytes)
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c16 * 8 + i;
+          p[i] = c < rows_valid ? ex2(fmaf(s[c], sl2, neg)) : 0.f;
+          l += p[i];
+        }
+        uint4 u;
+        u.x = pack2<BF16>(p[0], p[1]);
+        u.y = pack2<BF16>(p[2], p[3]);
+        u.z = pack2<BF16>(p[4], p[5]);
+        u.w = pack2<BF16>(p[6], p[7]);
+        const int chunk = c16 >> 3, unit = c16 & 7;
+        *reinterpret_cast<uint4*>(pb + chunk * (BM * 128) + ((unit ^ sw) << 4)) = u;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(&p_full[b]);
+    }
+    if (ok && !wait_bar_warp(g, &p_free[(n - 1) & 1], ((n - 1) >> 1) & 1, 8)) ok = false;
+    if (ok) {
+      tc_fence_after();
+      float o[HD];
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + O_COL + c * 32, v);
+        tmem_wait_ld();
+        reg_fence(v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      const int row = q0 + r;
+      if (row < a.n_q) {
+        const float inv = 1.f / l;
+        if (a.n_splits == 1) {
+          using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+          T* dst = reinterpret_cast<T*>(a.out) + ((int64_t)row * a.num_heads + h) * HD;
+          store_row<BF16>(dst, o, inv);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (((int64_t)split * a.n_q + row) * a.num_heads + h) * HD);
+#pragma unroll
+          for (int i = 0; i < HD / 4; ++i)
+            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+          a.part_lse[((int64_t)split * a.n_q + row) * a.num_heads + h] = m_ref + __log2f(l);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool configured_smem[2] = {false, false};
+
+}  // namespace
+
+bool tc_supported(int dtype, int head_dim, int num_heads, int page_size) {
+  return (dtype == 0 || dtype == 1) && head_dim == HD && num_heads >= 1 && page_size >= 1;
+}
+
+TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, int page_size, int num_heads,
+                       int head_dim, cudaError_t* err) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !tc_supported(dtype, head_dim, num_heads, page_size)) {
+    if (err) *err = cudaErrorNotSupported;
+    return nullptr;
+  }
+  TcMaps* m = new (std::nothrow) TcMaps();
+  if (!m) {
+    if (err) *err = cudaErrorMemoryAllocation;
+    return nullptr;
+  }
+  m->dtype = dtype;
+  m->num_heads = num_heads;
+  m->head_dim = head_dim;
+  const cuuint64_t row_bytes = (cuuint64_t)num_heads * head_dim * 2;
+  cuuint64_t dims[3] = {(cuuint64_t)num_heads * head_dim, (cuuint64_t)page_size,
+                        (cuuint64_t)num_blocks * max_pages * 2};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * page_size};
+  cuuint32_t box[3] = {HD, BN, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&m->cache, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   cache, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    delete m;
+    if (err) *err = cudaErrorInvalidValue;
+    return nullptr;
+  }
+  return m;
+}
+
+void tc_destroy_maps(TcMaps* m) { delete m; }
+
+cudaError_t launch_attn_tc(const AttnArgs& a, TcMaps* maps, int block, int max_pages, int dtype,
+                           cudaStream_t stream) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !maps || a.head_dim != HD) return cudaErrorNotSupported;
+  CUtensorMap qmap;
+  const cuuint64_t row_bytes = (cuuint64_t)a.num_heads * HD * 2;
+  cuuint64_t dims[2] = {(cuuint64_t)a.num_heads * HD, (cuuint64_t)a.n_q};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {HD, BM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&qmap, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   const_cast<void*>(a.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  dim3 grid((a.n_q + BM - 1) / BM, a.num_heads, a.n_splits);
+  const int page_base = block * max_pages;
+  if (dtype == 0) {
+    if (!configured_smem[0]) {
+      cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      configured_smem[0] = true;
+    }
+    attn_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, maps->cache, qmap, page_base);
+  } else {
+    if (!configured_smem[1]) {
+      cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      configured_smem[1] = true;
+    }
+    attn_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, maps->cache, qmap, page_base);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace kvc
