@@ -50,6 +50,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work")
+    p.add_argument("--layers", type=int, default=None,
+                   help="profiling size only: override the number of layers")
+    p.add_argument("--frames", type=int, default=None,
+                   help="profiling size only: override the stream length")
     return p.parse_args()
 
 
@@ -175,13 +179,22 @@ class Stream:
         return self.w.page_size * (s["scale_pages"] + s["live_pages"]) + s["special_tokens"]
 
 
+def workload(args):
+    from streaming_paged_kv_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.layers:
+        w = w.with_(num_layers=args.layers)
+    if args.frames:
+        w = w.with_(n_frames=args.frames)
+    return w
+
+
 def run_ours(args, rank, world):
     import torch
     from streaming_paged_kv_gb300 import build
     build.build()
     from streaming_paged_kv_gb300 import kvc
-    from streaming_paged_kv_gb300.workloads import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = workload(args)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     K = args.steps if args.steps is not None else w.n_frames - args.warmup
@@ -414,8 +427,7 @@ def run_reference(args):
     """The CPU oracle as the reference arm: each step is a bounded sample of a
     frame at the end of the stream (a slice of one layer's query rows),
     extrapolated to a whole frame."""
-    from streaming_paged_kv_gb300.workloads import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = workload(args)
     K = args.steps if args.steps is not None else 8
     W = args.warmup if args.warmup is not None else 3
     K, W = max(1, K), max(0, W)
@@ -461,9 +473,8 @@ def main():
         torch.distributed.init_process_group("nccl")
     res = run_ours(args, rank, world)
     if rank == 0:
-        from streaming_paged_kv_gb300.workloads import WORKLOADS
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(WORKLOADS[args.workload], args.seed, args.cpu_budget)
+            res["cpu_baseline"] = cpu_baseline(workload(args), args.seed, args.cpu_budget)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -15,14 +15,19 @@
 // for Streaming Inference with FlashInfer Integration"; [PERF] "How to Improve
 // Streaming Inference Performance with FlashInfer KV Cache Backend".
 //
-// CTA = one 128-row query tile x one head x one KV split.  Warps:
-//   0-3  softmax + epilogue: thread r owns query row r (TMEM lane r)
-//   4    TMA producer (one lane): Q once, then K/V tiles into a 3-stage ring
-//   5    MMA issuer (one lane): S = Q K^T into TMEM (double-buffered),
-//        O += P V into TMEM
-// Shared memory tiles use the 128-byte swizzle that both TMA and the tensor
-// core understand; P (bf16/f16) is written by the softmax threads into the
-// same swizzled K-major layout.  Scores live in the log2 domain (scaled by
+// CTA = two 128-row query tiles (Q0, Q1) x one head x one KV split; each K/V
+// tile is loaded once and serves both query tiles.  Warps:
+//   0-3  softmax + epilogue of Q0, 4-7 softmax + epilogue of Q1: thread r of a
+//        warpgroup owns query row r (TMEM lane r)
+//   8    TMA producer (one lane): Q0/Q1, then K/V tiles into a 4-stage ring
+//   9    MMA issuer (one lane): S_i = Q_i K^T into TMEM, O_i += P_i V with P_i
+//        read from TMEM
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
+// P0 [384,448) P1 [448,512); P holds two 16-bit values per column.
+// A warpgroup copies its S tile out of TMEM in one go and releases it at
+// once, so the next S MMA of its query tile runs while it computes the
+// exponentials.  Q and K/V tiles use the 128-byte swizzle that both TMA and
+// the tensor core understand.  Scores live in the log2 domain (scaled by
 // sm_scale * log2 e).  O is rescaled lazily: only when a row's running max
 // grows by more than 8 (a factor 256), otherwise P is taken against the stale
 // max, which fp32 accumulation absorbs.
@@ -53,25 +58,27 @@ struct TcMaps {
 
 namespace {
 
-constexpr int BM = 128;           // query rows per CTA
+constexpr int BM = 128;           // query rows per query tile
+constexpr int QT = 2;             // query tiles per CTA
 constexpr int BN = 128;           // KV rows per tile
 constexpr int HD = 64;            // head dim of this kernel
-constexpr int STAGES = 3;
-constexpr int NUM_THREADS = 192;
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 320;
+constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
 constexpr uint32_t TILE_BYTES = BN * HD * 2;         // 16 KB: one K or V tile
-constexpr uint32_t Q_BYTES = BM * HD * 2;            // 16 KB
-constexpr uint32_t P_BYTES = BM * BN * 2;            // 32 KB: two 64-column chunks
+constexpr uint32_t Q_BYTES = BM * HD * 2;            // 16 KB per query tile
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL0 = 0, O_COL = 256;
+__host__ __device__ constexpr uint32_t s_col(int i) { return i * BN; }
+__host__ __device__ constexpr uint32_t o_col(int i) { return 2 * BN + i * HD; }
+__host__ __device__ constexpr uint32_t p_col(int i) { return 2 * BN + 2 * HD + i * (BN / 2); }
 constexpr float RESCALE_THRESHOLD = 8.0f;            // log2 units
 constexpr long long kDrainBudget = 1LL << 26;        // cycles for draining after an abort
 
 // Shared memory map (offsets from a 1024-aligned base).
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
 constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
-constexpr uint32_t OFF_P = OFF_V + STAGES * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + STAGES * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
 
 // ------------------------------------------------------------- PTX helpers
@@ -235,6 +242,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -266,6 +282,41 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// MMA with A read from TMEM (two 16-bit elements per column, row m in lane m).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// Two fp32 FMAs / adds in one instruction.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 template <bool BF16>
 __device__ __forceinline__ void store_row(void* dst, const float* o, float inv) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -290,22 +341,24 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
   uint8_t* sQ = smem + OFF_Q;
   uint8_t* sK = smem + OFF_K;
   uint8_t* sV = smem + OFF_V;
-  uint8_t* sP = smem + OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* kv_full = bars + 1;                 // [STAGES]
   uint64_t* kv_empty = bars + 1 + STAGES;       // [STAGES]
-  uint64_t* s_full = bars + 1 + 2 * STAGES;     // [2]
-  uint64_t* p_full = bars + 3 + 2 * STAGES;     // [2]
-  uint64_t* p_free = bars + 5 + 2 * STAGES;     // [2]
-  uint64_t* drain = bars + 7 + 2 * STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * STAGES);
+  uint64_t* s_full = bars + 1 + 2 * STAGES;     // [QT] S_i written by the tensor core
+  uint64_t* s_free = bars + 3 + 2 * STAGES;     // [QT] S_i copied out by its warpgroup
+  uint64_t* p_full = bars + 5 + 2 * STAGES;     // [QT] P_i written (and O_i rescaled)
+  uint64_t* p_free = bars + 7 + 2 * STAGES;     // [QT] P_i V product done
+  uint64_t* drain = bars + 9 + 2 * STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10 + 2 * STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
-  const int q0 = qt * BM;
+  const int h = blockIdx.y, split = blockIdx.z;
+  const int q0 = blockIdx.x * (QT * BM);
+  const bool has_q1 = q0 + BM < a.n_q;
+  const int nq_tiles = has_q1 ? 2 : 1;
   const int t0 = (int)(((int64_t)split * a.n_tiles) / a.n_splits);
   const int t1 = (int)(((int64_t)(split + 1) * a.n_tiles) / a.n_splits);
   const int n = t1 - t0;
@@ -317,10 +370,11 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], BM);
-      mbar_init(&p_free[b], 1);
+    for (int i = 0; i < QT; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], BM);
+      mbar_init(&p_full[i], BM);
+      mbar_init(&p_free[i], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -338,12 +392,13 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0 && n > 0) {
       int issued = 0;
-      mbar_expect_tx(q_full, Q_BYTES);
+      mbar_expect_tx(q_full, nq_tiles * Q_BYTES);
       tma_load_2d(sQ, &q_map, h * HD, q0, q_full);
+      if (has_q1) tma_load_2d(sQ + Q_BYTES, &q_map, h * HD, q0 + BM, q_full);
       for (int j = 0; j < n; ++j) {
         const int st = j % STAGES;
         if (j >= STAGES && !wait_bar(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
@@ -361,40 +416,50 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
           drain_bar(&kv_full[j % STAGES], (j / STAGES) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t IDESC_S = idesc_f16(BM, BN, BF16, false);
       constexpr uint32_t IDESC_O = idesc_f16(BM, HD, BF16, true);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
-      bool ok = wait_bar(g, q_full, 0, 2);
-      auto issue_s = [&](int j) -> bool {
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      auto issue_s = [&](int i, int j) {
         const int st = j % STAGES;
-        if (!wait_bar(g, &kv_full[st], (j / STAGES) & 1, 3)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + S_COL0 + (j & 1) * BN;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k)
-          umma(d, sdesc_sw128(aQ + k * 32, 16, 1024), sdesc_sw128(aK + st * TILE_BYTES + k * 32, 16, 1024),
-               IDESC_S, k > 0);
-        umma_commit(&s_full[j & 1]);
-        return true;
+          umma(tmem + s_col(i), sdesc_sw128(aQ + i * Q_BYTES + k * 32, 16, 1024),
+               sdesc_sw128(aK + st * TILE_BYTES + k * 32, 16, 1024), IDESC_S, k > 0);
+        umma_commit(&s_full[i]);
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n && !issue_s(j + 1)) break;
-        const int b = j & 1, st = j % STAGES;
-        if (!wait_bar(g, &p_full[b], (j >> 1) & 1, 4)) break;
+      bool ok = wait_bar(g, q_full, 0, 2) && wait_bar(g, &kv_full[0], 0, 3);
+      if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint32_t a_addr = aP + b * P_BYTES + (k >> 2) * (BM * 128) + (k & 3) * 32;
-          const uint32_t b_addr = aV + st * TILE_BYTES + k * 16 * 128;
-          umma(tmem + O_COL, sdesc_sw128(a_addr, 16, 1024), sdesc_sw128(b_addr, BN * 128, 1024), IDESC_O,
-               (j > 0 || k > 0) ? 1u : 0u);
+        for (int i = 0; i < nq_tiles; ++i) issue_s(i, 0);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int st = j % STAGES;
+        if (j + 1 < n) {
+          // The next S of a query tile may start once its warpgroup has copied S out.
+          ok = wait_bar(g, &kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, 3);
+          for (int i = 0; ok && i < nq_tiles; ++i) {
+            ok = wait_bar(g, &s_free[i], j & 1, 4);
+            if (ok) {
+              tc_fence_after();
+              issue_s(i, j + 1);
+            }
+          }
         }
-        umma_commit(&kv_empty[st]);
-        umma_commit(&p_free[b]);
+        for (int i = 0; ok && i < nq_tiles; ++i) {
+          ok = wait_bar(g, &p_full[i], j & 1, 5);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            umma_ts(tmem + o_col(i), tmem + p_col(i) + k * 8,
+                    sdesc_sw128(aV + st * TILE_BYTES + k * 16 * 128, BN * 128, 1024), IDESC_O,
+                    (j > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&p_free[i]);
+        }
+        if (ok) umma_commit(&kv_empty[st]);
       }
       // Every MMA this thread issued has completed once `drain` flips.
       umma_commit(drain);
@@ -402,95 +467,112 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
     }
   } else {
     // ------------------------------------------------ softmax + epilogue
-    const int r = threadIdx.x;                       // query row within the tile == TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int qi = warp >> 2;                        // query tile of this warpgroup
+    const int r = threadIdx.x & (BM - 1);            // query row within the tile == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t S_ = lane_base + s_col(qi), O_ = lane_base + o_col(qi), P_ = lane_base + p_col(qi);
     const float sl2 = a.sm_scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = n > 0;
-    uint8_t* prow = sP + r * 128;
-    const int sw = r & 7;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    float m_ref = -INFINITY;
+    uint64_t l2 = 0;                                 // two partial row sums
+    bool ok = n > 0 && qi < nq_tiles;
     for (int j = 0; ok && j < n; ++j) {
-      const int b = j & 1;
       const int rows_valid = a.tiles[t0 + j].rows;
-      if (!wait_bar_warp(g, &s_full[b], (j >> 1) & 1, 5)) { ok = false; break; }
+      if (!wait_bar_warp(g, &s_full[qi], j & 1, 6)) { ok = false; break; }
       tc_fence_after();
-      float s[BN];
+      const bool partial = rows_valid < BN;
+      // Pass 1: row max, four independent chains over the 32-column chunks.
+      float mxk[4];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_base + S_COL0 + b * BN + c * 32, v);
+        tmem_ld32(S_ + c * 32, v);
         tmem_wait_ld();
         reg_fence(v);
+        if (partial) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= rows_valid) v[i] = __float_as_uint(-INFINITY);
+        }
+        float m = __uint_as_float(v[0]);
+#pragma unroll
+        for (int i = 1; i < 31; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+        mxk[c] = fmaxf(m, __uint_as_float(v[31]));
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, c < rows_valid ? s[c] : -INFINITY);
-      const float m_tile = mx * sl2;
+      const float m_tile = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])) * sl2;
       const bool need = m_tile > m_ref + RESCALE_THRESHOLD;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? fmaxf(m_ref, m_tile) : m_ref;
         const float alpha = ex2(m_ref - m_new);      // 0 on the first tile
         if (j > 0) {
           // The previous P V product must have landed before O is rescaled.
-          if (!wait_bar_warp(g, &p_free[b ^ 1], ((j - 1) >> 1) & 1, 6)) { ok = false; break; }
+          if (!wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 7)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t v[32];
-            tmem_ld32(lane_base + O_COL + c * 32, v);
+            tmem_ld32(O_ + c * 32, v);
             tmem_wait_ld();
             reg_fence(v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(lane_base + O_COL + c * 32, v);
+            tmem_st32(O_ + c * 32, v);
           }
           tmem_wait_st();
         }
-        l *= alpha;
+        l2 = f2_pack(f2_lo(l2) * alpha, f2_hi(l2) * alpha);
         m_ref = m_new;
       }
-      // P buffer b is free once the P V product of tile j-2 has completed.
-      if (j >= 2 && !wait_bar_warp(g, &p_free[b], ((j - 2) >> 1) & 1, 7)) { ok = false; break; }
-      const float neg = -m_ref;
-      uint8_t* pb = prow + b * P_BYTES;
+      // P_i is free once the P V product of the previous tile has completed.
+      if (j > 0 && !wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 8)) { ok = false; break; }
+      const uint64_t negx2 = f2_pack(-m_ref, -m_ref);
+      // Pass 2: P = 2^(s*sl2 - m) chunk by chunk into TMEM; S is released
+      // as soon as its last chunk has been read.
 #pragma unroll
-      for (int c16 = 0; c16 < BN / 8; ++c16) {       // 16 chunks of 8 columns (16 bytes)
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c16 * 8 + i;
-          p[i] = c < rows_valid ? ex2(fmaf(s[c], sl2, neg)) : 0.f;
-          l += p[i];
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(S_ + c * 32, v);
+        tmem_wait_ld();
+        reg_fence(v);
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&s_free[qi]);                  // the tensor core may overwrite S now
         }
-        uint4 u;
-        u.x = pack2<BF16>(p[0], p[1]);
-        u.y = pack2<BF16>(p[2], p[3]);
-        u.z = pack2<BF16>(p[4], p[5]);
-        u.w = pack2<BF16>(p[6], p[7]);
-        const int chunk = c16 >> 3, unit = c16 & 7;
-        *reinterpret_cast<uint4*>(pb + chunk * (BM * 128) + ((unit ^ sw) << 4)) = u;
+        if (partial) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= rows_valid) v[i] = __float_as_uint(-INFINITY);
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t x = ffma2(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2x2, negx2);
+          const float p0 = ex2(f2_lo(x)), p1 = ex2(f2_hi(x));
+          l2 = fadd2(l2, f2_pack(p0, p1));
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        tmem_st16(P_ + c * 16, pk);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[qi]);
     }
-    if (ok && !wait_bar_warp(g, &p_free[(n - 1) & 1], ((n - 1) >> 1) & 1, 8)) ok = false;
+    if (ok && !wait_bar_warp(g, &p_free[qi], (n - 1) & 1, 9)) ok = false;
     if (ok) {
       tc_fence_after();
       float o[HD];
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_base + O_COL + c * 32, v);
+        tmem_ld32(O_ + c * 32, v);
         tmem_wait_ld();
         reg_fence(v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(v[i]);
       }
-      const int row = q0 + r;
+      const int row = q0 + qi * BM + r;
       if (row < a.n_q) {
+        const float l = f2_lo(l2) + f2_hi(l2);
         const float inv = 1.f / l;
         if (a.n_splits == 1) {
           using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
@@ -591,7 +673,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, TcMaps* maps, int block, int max_p
                    const_cast<void*>(a.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  dim3 grid((a.n_q + BM - 1) / BM, a.num_heads, a.n_splits);
+  dim3 grid((a.n_q + QT * BM - 1) / (QT * BM), a.num_heads, a.n_splits);
   const int page_base = block * max_pages;
   if (dtype == 0) {
     if (!configured_smem[0]) {

@@ -83,7 +83,7 @@ int simt_tile_rows(int head_dim);
 // kvc_attn_tc.cu
 bool tc_supported(int dtype, int head_dim, int num_heads, int page_size);
 constexpr int kTcTileRows = 128;
-constexpr int kTcQRows = 128;
+constexpr int kTcQRows = 256;   // query rows per CTA of the tensor-core kernel
 struct TcMaps;   // opaque: TMA descriptors of the cache (per handle)
 TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, int page_size,
                        int num_heads, int head_dim, cudaError_t* err);
