@@ -437,18 +437,17 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       }
       for (int j = 0; ok && j < n; ++j) {
         const int st = j % STAGES;
-        if (j + 1 < n) {
-          // The next S of a query tile may start once its warpgroup has copied S out.
-          ok = wait_bar(g, &kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, 3);
-          for (int i = 0; ok && i < nq_tiles; ++i) {
-            ok = wait_bar(g, &s_free[i], j & 1, 4);
-            if (ok) {
-              tc_fence_after();
-              issue_s(i, j + 1);
-            }
-          }
-        }
+        if (j + 1 < n) ok = wait_bar(g, &kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, 3);
+        // Per query tile: its next S as soon as its warpgroup has copied S out,
+        // then its P V product once P is in TMEM.  The two warpgroups settle
+        // into alternating with each other on the tensor core.
         for (int i = 0; ok && i < nq_tiles; ++i) {
+          if (j + 1 < n) {
+            ok = wait_bar(g, &s_free[i], j & 1, 4);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(i, j + 1);
+          }
           ok = wait_bar(g, &p_full[i], j & 1, 5);
           if (!ok) break;
           tc_fence_after();
@@ -481,23 +480,29 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       if (!wait_bar_warp(g, &s_full[qi], j & 1, 6)) { ok = false; break; }
       tc_fence_after();
       const bool partial = rows_valid < BN;
-      // Pass 1: row max, four independent chains over the 32-column chunks.
+      // Pass 1: row max; two TMEM loads in flight, one chain per 32-column chunk.
       float mxk[4];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(S_ + c * 32, v);
+      for (int c2 = 0; c2 < BN / 64; ++c2) {
+        uint32_t v[2][32];
+        tmem_ld32(S_ + c2 * 64, v[0]);
+        tmem_ld32(S_ + c2 * 64 + 32, v[1]);
         tmem_wait_ld();
-        reg_fence(v);
-        if (partial) {
+        reg_fence(v[0]);
+        reg_fence(v[1]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= rows_valid) v[i] = __float_as_uint(-INFINITY);
+        for (int u = 0; u < 2; ++u) {
+          const int c = 2 * c2 + u;
+          if (partial) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= rows_valid) v[u][i] = __float_as_uint(-INFINITY);
+          }
+          float m = __uint_as_float(v[u][0]);
+#pragma unroll
+          for (int i = 1; i < 31; i += 2) m = fmax3(m, __uint_as_float(v[u][i]), __uint_as_float(v[u][i + 1]));
+          mxk[c] = fmaxf(m, __uint_as_float(v[u][31]));
         }
-        float m = __uint_as_float(v[0]);
-#pragma unroll
-        for (int i = 1; i < 31; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-        mxk[c] = fmaxf(m, __uint_as_float(v[31]));
       }
       const float m_tile = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])) * sl2;
       const bool need = m_tile > m_ref + RESCALE_THRESHOLD;
@@ -526,32 +531,39 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       // P_i is free once the P V product of the previous tile has completed.
       if (j > 0 && !wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 8)) { ok = false; break; }
       const uint64_t negx2 = f2_pack(-m_ref, -m_ref);
-      // Pass 2: P = 2^(s*sl2 - m) chunk by chunk into TMEM; S is released
-      // as soon as its last chunk has been read.
+      // Pass 2: P = 2^(s*sl2 - m) chunk by chunk into TMEM, loading chunk c+1
+      // while chunk c is computed; S is released once its last chunk is read.
+      uint32_t v[2][32];
+      tmem_ld32(S_, v[0]);
+      tmem_wait_ld();
+      reg_fence(v[0]);
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(S_ + c * 32, v);
-        tmem_wait_ld();
-        reg_fence(v);
-        if (c == BN / 32 - 1) {
+        uint32_t (&cur)[32] = v[c & 1];
+        if (c + 1 < BN / 32) {
+          tmem_ld32(S_ + (c + 1) * 32, v[(c + 1) & 1]);
+        } else {
           tc_fence_before();
           mbar_arrive(&s_free[qi]);                  // the tensor core may overwrite S now
         }
         if (partial) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= rows_valid) v[i] = __float_as_uint(-INFINITY);
+            if (c * 32 + i >= rows_valid) cur[i] = __float_as_uint(-INFINITY);
         }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint64_t x = ffma2(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2x2, negx2);
+          const uint64_t x = ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), sl2x2, negx2);
           const float p0 = ex2(f2_lo(x)), p1 = ex2(f2_hi(x));
           l2 = fadd2(l2, f2_pack(p0, p1));
           pk[i] = pack2<BF16>(p0, p1);
         }
         tmem_st16(P_ + c * 16, pk);
+        if (c + 1 < BN / 32) {
+          tmem_wait_ld();
+          reg_fence(v[(c + 1) & 1]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
