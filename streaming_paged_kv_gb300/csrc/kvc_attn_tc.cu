@@ -242,6 +242,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -315,6 +326,17 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t scale_pair(uint32_t packed, float alpha) {
+  if constexpr (BF16) {
+    __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&packed);
+    return pack2<true>(__low2float(t) * alpha, __high2float(t) * alpha);
+  } else {
+    __half2 t = *reinterpret_cast<__half2*>(&packed);
+    return pack2<false>(__low2float(t) * alpha, __high2float(t) * alpha);
+  }
 }
 
 template <bool BF16>
@@ -475,64 +497,21 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
     float m_ref = -INFINITY;
     uint64_t l2 = 0;                                 // two partial row sums
     bool ok = n > 0 && qi < nq_tiles;
+    int rows_next = n > 0 ? a.tiles[t0].rows : 0;
     for (int j = 0; ok && j < n; ++j) {
-      const int rows_valid = a.tiles[t0 + j].rows;
+      const int rows_valid = rows_next;
+      if (j + 1 < n) rows_next = a.tiles[t0 + j + 1].rows;   // prefetch for the next tile
       if (!wait_bar_warp(g, &s_full[qi], j & 1, 6)) { ok = false; break; }
       tc_fence_after();
       const bool partial = rows_valid < BN;
-      // Pass 1: row max; two TMEM loads in flight, one chain per 32-column chunk.
-      float mxk[4];
-#pragma unroll
-      for (int c2 = 0; c2 < BN / 64; ++c2) {
-        uint32_t v[2][32];
-        tmem_ld32(S_ + c2 * 64, v[0]);
-        tmem_ld32(S_ + c2 * 64 + 32, v[1]);
-        tmem_wait_ld();
-        reg_fence(v[0]);
-        reg_fence(v[1]);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = 2 * c2 + u;
-          if (partial) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c * 32 + i >= rows_valid) v[u][i] = __float_as_uint(-INFINITY);
-          }
-          float m = __uint_as_float(v[u][0]);
-#pragma unroll
-          for (int i = 1; i < 31; i += 2) m = fmax3(m, __uint_as_float(v[u][i]), __uint_as_float(v[u][i + 1]));
-          mxk[c] = fmaxf(m, __uint_as_float(v[u][31]));
-        }
-      }
-      const float m_tile = fmaxf(fmaxf(mxk[0], mxk[1]), fmaxf(mxk[2], mxk[3])) * sl2;
-      const bool need = m_tile > m_ref + RESCALE_THRESHOLD;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? fmaxf(m_ref, m_tile) : m_ref;
-        const float alpha = ex2(m_ref - m_new);      // 0 on the first tile
-        if (j > 0) {
-          // The previous P V product must have landed before O is rescaled.
-          if (!wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 7)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(O_ + c * 32, v);
-            tmem_wait_ld();
-            reg_fence(v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(O_ + c * 32, v);
-          }
-          tmem_wait_st();
-        }
-        l2 = f2_pack(f2_lo(l2) * alpha, f2_hi(l2) * alpha);
-        m_ref = m_new;
-      }
-      // P_i is free once the P V product of the previous tile has completed.
+      // P_i is free (and O_i stable) once the P V product of the previous tile has completed.
       if (j > 0 && !wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 8)) { ok = false; break; }
-      const uint64_t negx2 = f2_pack(-m_ref, -m_ref);
-      // Pass 2: P = 2^(s*sl2 - m) chunk by chunk into TMEM, loading chunk c+1
-      // while chunk c is computed; S is released once its last chunk is read.
+      // One pass over S in 32-column chunks, loading chunk c+1 while chunk c is
+      // computed.  Each chunk is exponentiated against the running reference
+      // m_ref; only when a chunk's max exceeds m_ref by more than the threshold
+      // (always on the first chunk of a row, rarely later) does the warp move
+      // the reference and rescale what was accumulated against the old one:
+      // O, l and the P chunks of this tile already in TMEM.
       uint32_t v[2][32];
       tmem_ld32(S_, v[0]);
       tmem_wait_ld();
@@ -551,6 +530,45 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i >= rows_valid) cur[i] = __float_as_uint(-INFINITY);
         }
+        float cm = __uint_as_float(cur[0]);
+#pragma unroll
+        for (int i = 1; i < 31; i += 2) cm = fmax3(cm, __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
+        cm = fmaxf(cm, __uint_as_float(cur[31])) * sl2;
+        const bool need = cm > m_ref + RESCALE_THRESHOLD;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? cm : m_ref;
+          const float alpha = ex2(m_ref - m_new);    // 0 while nothing has been accumulated
+          if (j > 0) {
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(O_ + cc * 32, o);
+              tmem_wait_ld();
+              reg_fence(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(O_ + cc * 32, o);
+            }
+          }
+          if (c > 0) {
+            tmem_wait_st();                          // this tile's earlier P chunks have landed
+#pragma unroll
+            for (int cc = 0; cc < c; ++cc) {
+              uint32_t pv[16];
+              tmem_ld16(P_ + cc * 16, pv);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                asm volatile("" : "+r"(pv[i])::"memory");
+                pv[i] = scale_pair<BF16>(pv[i], alpha);
+              }
+              tmem_st16(P_ + cc * 16, pv);
+            }
+          }
+          l2 = f2_pack(f2_lo(l2) * alpha, f2_hi(l2) * alpha);
+          m_ref = m_new;
+        }
+        const uint64_t negx2 = f2_pack(-m_ref, -m_ref);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

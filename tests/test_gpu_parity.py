@@ -186,3 +186,36 @@ def test_stale_plan_detected(kvc):
     c.run(1, qd, torch.empty_like(qd))
     assert kvc.kvc_device_status(c.h, c._stream()) == 0
     c.close()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_max_jumps_inside_and_across_tiles(kvc, kernel):
+    """Scores that jump far above the running max late in a tile (earlier P
+    chunks of that tile must be rescaled) and in a late tile (O must be
+    rescaled): a few keys are scaled up by 30 -- one patch row deep inside the
+    first page, and the special rows of the newest frame, which come last."""
+    from oracle import OraclePagedKV, paged_attention
+    from streaming_paged_kv_gb300.inputs import frame_qkv, to_bits
+    w = WORKLOADS["s224"]
+    _kernel_or_skip(kvc, w, kernel)
+    c = kvc.PagedKVCache(1, 16, 64, 256, "bf16", max_total_frames=64)
+    c.set_option(kvc.KVC_OPT_ATTN_KERNEL, kernel)
+    orc = OraclePagedKV(1, 256, 16, 64, "bf16", 8, 64, 16, 64)
+    for f in range(6):
+        q, k, v = frame_qkv(11, 2, f, 0, 256, 16, 64)
+        k = k.float()
+        if f == 0:
+            k[6 + 100] *= 30.0          # patch row 100 of the first page: chunk 3 of tile 0
+        if f == 5:
+            k[:6] *= 30.0               # newest specials: the last tile
+        k = k.to(torch.bfloat16)
+        c.append_frame(0, k.cuda(), v.cuda())
+        orc.append_frame(0, to_bits(k), to_bits(v))
+    c.plan()
+    qd = q.cuda()
+    out = torch.empty_like(qd)
+    c.run(0, qd, out)
+    want = paged_attention(orc, 0, to_bits(q))
+    torch.cuda.synchronize()
+    mx, rel = compare(out, want, "bf16")
+    assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
