@@ -17,20 +17,23 @@
 //
 // CTA = two 128-row query tiles (Q0, Q1) x one head x one KV split; each K/V
 // tile is loaded once and serves both query tiles.  Warps:
-//   0-3  softmax + epilogue of Q0, 4-7 softmax + epilogue of Q1: thread r of a
-//        warpgroup owns query row r (TMEM lane r)
-//   8    TMA producer (one lane): Q0/Q1, then K/V tiles into a 4-stage ring
-//   9    MMA issuer (one lane): S_i = Q_i K^T into TMEM, O_i += P_i V with P_i
-//        read from TMEM
+//   0-7   softmax + epilogue of Q0, 8-15 softmax + epilogue of Q1.  Within a
+//         query tile, warp w owns TMEM lanes [32(w%4), +32) (query rows) and
+//         columns [64 h, +64) of each S tile, h = (w/4)%2: two warps share
+//         every row, each holding half of its scores
+//   16    TMA producer (one lane): Q0/Q1, then K/V tiles into a 4-stage ring
+//   17    MMA issuer (one lane): S_i = Q_i K^T into TMEM, O_i += P_i V with P_i
+//         read from TMEM
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 // P0 [384,448) P1 [448,512); P holds two 16-bit values per column.
-// A warpgroup copies its S tile out of TMEM in one go and releases it at
-// once, so the next S MMA of its query tile runs while it computes the
-// exponentials.  Q and K/V tiles use the 128-byte swizzle that both TMA and
-// the tensor core understand.  Scores live in the log2 domain (scaled by
-// sm_scale * log2 e).  O is rescaled lazily: only when a row's running max
-// grows by more than 8 (a factor 256), otherwise P is taken against the stale
-// max, which fp32 accumulation absorbs.
+// Q and K/V tiles use the 128-byte swizzle that both TMA and the tensor core
+// understand.  Scores live in the log2 domain (scaled by sm_scale * log2 e).
+// Each warp exponentiates its half of the row against the running reference
+// max m_ref of the row.  The reference moves only when a score exceeds it by
+// more than 8 (a factor 256): then the two warps of the row agree on the new
+// reference through shared memory, recompute that tile's P from S and rescale
+// O and the row sums.  Otherwise P is taken against the stale reference, which
+// fp32 accumulation absorbs.
 //
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
 // the fact in the status word, raises a CTA-wide abort flag, and every role
@@ -63,8 +66,9 @@ constexpr int QT = 2;             // query tiles per CTA
 constexpr int BN = 128;           // KV rows per tile
 constexpr int HD = 64;            // head dim of this kernel
 constexpr int STAGES = 4;
-constexpr int NUM_THREADS = 320;
-constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
+constexpr int NUM_THREADS = 576;
+constexpr int PRODUCER_WARP = 16, MMA_WARP = 17;
+constexpr int SOFTMAX_THREADS = 2 * BM;              // per query tile: two warps per row
 constexpr uint32_t TILE_BYTES = BN * HD * 2;         // 16 KB: one K or V tile
 constexpr uint32_t Q_BYTES = BM * HD * 2;            // 16 KB per query tile
 constexpr uint32_t TMEM_COLS = 512;
@@ -79,7 +83,10 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
 constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + STAGES * TILE_BYTES;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+// Row exchange between the two warps of a row: [pair][warp half][slot][33 floats].
+constexpr uint32_t OFF_XCH = OFF_BAR + 256;
+constexpr uint32_t XCH_BYTES = 8 * 2 * 2 * 33 * 4;
+constexpr uint32_t SMEM_BYTES = OFF_XCH + XCH_BYTES + 1024;  // + alignment slack
 
 // ------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -177,6 +184,22 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// One lane of a converged warp (elect.sync), the same lane every time.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Named barrier over `count` threads (the two warps of a row pair).
+__device__ __forceinline__ void pair_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
@@ -394,8 +417,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
     }
     for (int i = 0; i < QT; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], BM);
-      mbar_init(&p_full[i], BM);
+      mbar_init(&s_free[i], SOFTMAX_THREADS);
+      mbar_init(&p_full[i], SOFTMAX_THREADS);
       mbar_init(&p_free[i], 1);
     }
     mbar_init(drain, 1);
@@ -416,23 +439,29 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0 && n > 0) {
+    // The whole warp runs the loop and its waits; one elected lane issues.
+    if (n > 0) {
+      const bool leader = elect_one();
       int issued = 0;
-      mbar_expect_tx(q_full, nq_tiles * Q_BYTES);
-      tma_load_2d(sQ, &q_map, h * HD, q0, q_full);
-      if (has_q1) tma_load_2d(sQ + Q_BYTES, &q_map, h * HD, q0 + BM, q_full);
+      if (leader) {
+        mbar_expect_tx(q_full, nq_tiles * Q_BYTES);
+        tma_load_2d(sQ, &q_map, h * HD, q0, q_full);
+        if (has_q1) tma_load_2d(sQ + Q_BYTES, &q_map, h * HD, q0 + BM, q_full);
+      }
       for (int j = 0; j < n; ++j) {
         const int st = j % STAGES;
-        if (j >= STAGES && !wait_bar(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
+        if (j >= STAGES && !wait_bar_warp(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
         const KvTile tile = a.tiles[t0 + j];
         const int plane = (page_base + tile.page) * 2;
-        mbar_expect_tx(&kv_full[st], 2 * TILE_BYTES);
-        tma_load_3d(sK + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane, &kv_full[st]);
-        tma_load_3d(sV + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
+        if (leader) {
+          mbar_expect_tx(&kv_full[st], 2 * TILE_BYTES);
+          tma_load_3d(sK + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane, &kv_full[st]);
+          tma_load_3d(sV + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
+        }
         issued = j + 1;
       }
-      if (*abort_flag) {
-        // Let every copy this thread started land before the CTA exits.
+      if (*abort_flag && leader) {
+        // Let every copy this warp started land before the CTA exits.
         drain_bar(q_full, 0);
         for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
           drain_bar(&kv_full[j % STAGES], (j / STAGES) & 1);
@@ -440,183 +469,231 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0 && n > 0) {
+    // The whole warp runs the loop and its waits with warp-uniform values;
+    // one elected lane issues the MMAs and the commits.
+    if (n > 0) {
+      const bool leader = elect_one();
       constexpr uint32_t IDESC_S = idesc_f16(BM, BN, BF16, false);
       constexpr uint32_t IDESC_O = idesc_f16(BM, HD, BF16, true);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      // Descriptors are built once; a step along K or to another stage only
+      // adds to the start-address field (address >> 4, 14 bits, no carry for
+      // shared-memory addresses below 256 KB), so each MMA costs one add.
+      const uint64_t dQ[QT] = {sdesc_sw128(smem_u32(sQ), 16, 1024), sdesc_sw128(smem_u32(sQ) + Q_BYTES, 16, 1024)};
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
+      constexpr uint64_t STAGE_STEP = TILE_BYTES >> 4;     // next K/V stage
+      constexpr uint64_t K16_STEP = 32 >> 4;               // 16 bf16 along K inside a 128-byte row
+      constexpr uint64_t V16_STEP = (16 * 128) >> 4;       // 16 rows of V
       auto issue_s = [&](int i, int j) {
-        const int st = j % STAGES;
+        const uint64_t dK = dK0 + (uint64_t)(j % STAGES) * STAGE_STEP;
+        const uint32_t d = tmem + s_col(i);
+        if (leader) {
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k)
-          umma(tmem + s_col(i), sdesc_sw128(aQ + i * Q_BYTES + k * 32, 16, 1024),
-               sdesc_sw128(aK + st * TILE_BYTES + k * 32, 16, 1024), IDESC_S, k > 0);
-        umma_commit(&s_full[i]);
+          for (int k = 0; k < HD / 16; ++k)
+            umma(d, dQ[i] + k * K16_STEP, dK + k * K16_STEP, IDESC_S, k > 0);
+          umma_commit(&s_full[i]);
+        }
+        __syncwarp();
       };
-      bool ok = wait_bar(g, q_full, 0, 2) && wait_bar(g, &kv_full[0], 0, 3);
+      bool ok = wait_bar_warp(g, q_full, 0, 2) && wait_bar_warp(g, &kv_full[0], 0, 3);
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < nq_tiles; ++i) issue_s(i, 0);
       }
       for (int j = 0; ok && j < n; ++j) {
         const int st = j % STAGES;
-        if (j + 1 < n) ok = wait_bar(g, &kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, 3);
-        // Per query tile: its next S as soon as its warpgroup has copied S out,
-        // then its P V product once P is in TMEM.  The two warpgroups settle
-        // into alternating with each other on the tensor core.
+        if (j + 1 < n) ok = wait_bar_warp(g, &kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, 3);
+        // Per query tile: its next S as soon as its warps have copied S out,
+        // then its P V product once P is in TMEM.
         for (int i = 0; ok && i < nq_tiles; ++i) {
           if (j + 1 < n) {
-            ok = wait_bar(g, &s_free[i], j & 1, 4);
+            ok = wait_bar_warp(g, &s_free[i], j & 1, 4);
             if (!ok) break;
             tc_fence_after();
             issue_s(i, j + 1);
           }
-          ok = wait_bar(g, &p_full[i], j & 1, 5);
+          ok = wait_bar_warp(g, &p_full[i], j & 1, 5);
           if (!ok) break;
           tc_fence_after();
+          const uint64_t dV = dV0 + (uint64_t)st * STAGE_STEP;
+          const uint32_t o = tmem + o_col(i), pa = tmem + p_col(i);
+          if (leader) {
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            umma_ts(tmem + o_col(i), tmem + p_col(i) + k * 8,
-                    sdesc_sw128(aV + st * TILE_BYTES + k * 16 * 128, BN * 128, 1024), IDESC_O,
-                    (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&p_free[i]);
+            for (int k = 0; k < BN / 16; ++k)
+              umma_ts(o, pa + k * 8, dV + k * V16_STEP, IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+            umma_commit(&p_free[i]);
+          }
+          __syncwarp();
         }
-        if (ok) umma_commit(&kv_empty[st]);
+        if (ok && leader) umma_commit(&kv_empty[st]);
+        __syncwarp();
       }
-      // Every MMA this thread issued has completed once `drain` flips.
-      umma_commit(drain);
-      drain_bar(drain, 0);
+      // Every MMA this warp issued has completed once `drain` flips.
+      if (leader) {
+        umma_commit(drain);
+        drain_bar(drain, 0);
+      }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------ softmax + epilogue
-    const int qi = warp >> 2;                        // query tile of this warpgroup
-    const int r = threadIdx.x & (BM - 1);            // query row within the tile == TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t S_ = lane_base + s_col(qi), O_ = lane_base + o_col(qi), P_ = lane_base + p_col(qi);
+    const int qi = warp >> 3;                        // query tile of this warp
+    const int half = (warp >> 2) & 1;                // which 64 columns of each S tile
+    const int quarter = warp & 3;                    // TMEM lanes [32 quarter, +32)
+    const int pair = qi * 4 + quarter;               // the two warps sharing these rows
+    const int r = quarter * 32 + lane;               // query row within the tile == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t S_ = lane_base + s_col(qi) + half * 64;
+    const uint32_t P_ = lane_base + p_col(qi) + half * 32;
+    const uint32_t O_ = lane_base + o_col(qi);
+    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
+    float* mine = xch + (pair * 2 + half) * 66;      // two slots of 33
+    float* theirs = xch + (pair * 2 + (half ^ 1)) * 66;
+    const int bar_id = 1 + pair;
+    const int col0 = half * 64;
     const float sl2 = a.sm_scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     float m_ref = -INFINITY;
-    uint64_t l2 = 0;                                 // two partial row sums
-    bool ok = n > 0 && qi < nq_tiles;
-    int rows_next = n > 0 ? a.tiles[t0].rows : 0;
-    for (int j = 0; ok && j < n; ++j) {
-      const int rows_valid = rows_next;
-      if (j + 1 < n) rows_next = a.tiles[t0 + j + 1].rows;   // prefetch for the next tile
-      if (!wait_bar_warp(g, &s_full[qi], j & 1, 6)) { ok = false; break; }
-      tc_fence_after();
-      const bool partial = rows_valid < BN;
-      // P_i is free (and O_i stable) once the P V product of the previous tile has completed.
-      if (j > 0 && !wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 8)) { ok = false; break; }
-      // One pass over S in 32-column chunks, loading chunk c+1 while chunk c is
-      // computed.  Each chunk is exponentiated against the running reference
-      // m_ref; only when a chunk's max exceeds m_ref by more than the threshold
-      // (always on the first chunk of a row, rarely later) does the warp move
-      // the reference and rescale what was accumulated against the old one:
-      // O, l and the P chunks of this tile already in TMEM.
-      uint32_t v[2][32];
-      tmem_ld32(S_, v[0]);
-      tmem_wait_ld();
-      reg_fence(v[0]);
+    uint64_t la = 0, lb = 0;                         // row-sum partials over this warp's columns
+    bool ok = n > 0 && qi < nq_tiles;                // the same for both warps of a pair
+
+    // P for this warp's 64 columns of tile S into TMEM, against reference m:
+    // returns the partial sums; clamps the exponent so that a stale reference
+    // can never produce inf (such tiles are recomputed).
+    auto make_p = [&](int rows_valid, float m, uint64_t& ta, uint64_t& tb, float* smax) {
+      const uint64_t negx2 = f2_pack(-m, -m);
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t (&cur)[32] = v[c & 1];
-        if (c + 1 < BN / 32) {
-          tmem_ld32(S_ + (c + 1) * 32, v[(c + 1) & 1]);
-        } else {
-          tc_fence_before();
-          mbar_arrive(&s_free[qi]);                  // the tensor core may overwrite S now
-        }
-        if (partial) {
+      for (int u = 0; u < 2; ++u) {
+        uint32_t v[32];
+        tmem_ld32(S_ + u * 32, v);
+        tmem_wait_ld();
+        reg_fence(v);
+        if (rows_valid < col0 + 64) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= rows_valid) cur[i] = __float_as_uint(-INFINITY);
+            if (col0 + u * 32 + i >= rows_valid) v[i] = __float_as_uint(-INFINITY);
         }
-        float cm = __uint_as_float(cur[0]);
-#pragma unroll
-        for (int i = 1; i < 31; i += 2) cm = fmax3(cm, __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
-        cm = fmaxf(cm, __uint_as_float(cur[31])) * sl2;
-        const bool need = cm > m_ref + RESCALE_THRESHOLD;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? cm : m_ref;
-          const float alpha = ex2(m_ref - m_new);    // 0 while nothing has been accumulated
-          if (j > 0) {
-#pragma unroll
-            for (int cc = 0; cc < HD / 32; ++cc) {
-              uint32_t o[32];
-              tmem_ld32(O_ + cc * 32, o);
-              tmem_wait_ld();
-              reg_fence(o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(O_ + cc * 32, o);
-            }
-          }
-          if (c > 0) {
-            tmem_wait_st();                          // this tile's earlier P chunks have landed
-#pragma unroll
-            for (int cc = 0; cc < c; ++cc) {
-              uint32_t pv[16];
-              tmem_ld16(P_ + cc * 16, pv);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                asm volatile("" : "+r"(pv[i])::"memory");
-                pv[i] = scale_pair<BF16>(pv[i], alpha);
-              }
-              tmem_st16(P_ + cc * 16, pv);
-            }
-          }
-          l2 = f2_pack(f2_lo(l2) * alpha, f2_hi(l2) * alpha);
-          m_ref = m_new;
-        }
-        const uint64_t negx2 = f2_pack(-m_ref, -m_ref);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint64_t x = ffma2(f2_pack(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), sl2x2, negx2);
-          const float p0 = ex2(f2_lo(x)), p1 = ex2(f2_hi(x));
-          l2 = fadd2(l2, f2_pack(p0, p1));
+          const float s0 = __uint_as_float(v[2 * i]), s1 = __uint_as_float(v[2 * i + 1]);
+          if (smax) *smax = fmax3(*smax, s0, s1);
+          const uint64_t x = ffma2(f2_pack(s0, s1), sl2x2, negx2);
+          const float p0 = ex2(fminf(f2_lo(x), 120.f)), p1 = ex2(fminf(f2_hi(x), 120.f));
+          if (i & 1) tb = fadd2(tb, f2_pack(p0, p1));
+          else ta = fadd2(ta, f2_pack(p0, p1));
           pk[i] = pack2<BF16>(p0, p1);
         }
-        tmem_st16(P_ + c * 16, pk);
-        if (c + 1 < BN / 32) {
-          tmem_wait_ld();
-          reg_fence(v[(c + 1) & 1]);
-        }
+        tmem_st16(P_ + u * 16, pk);
       }
+    };
+
+    int rows_next = ok ? a.tiles[t0].rows : 0;
+    for (int j = 0; ok && j < n; ++j) {
+      const int rows_valid = rows_next;
+      if (j + 1 < n) rows_next = a.tiles[t0 + j + 1].rows;   // prefetch for the next tile
+      bool good = wait_bar_warp(g, &s_full[qi], j & 1, 6);
+      // P_i is free (and O_i stable) once the P V product of the previous tile has completed.
+      if (good && j > 0) good = wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 8);
+      uint64_t ta = 0, tb = 0;
+      float smax = -INFINITY;
+      if (good) {
+        tc_fence_after();
+        make_p(rows_valid, m_ref, ta, tb, &smax);
+      }
+      // Tell the other warp of these rows whether the reference has to move
+      // (or whether this warp gave up), and this row's score max.
+      const float mx = smax * sl2;
+      const bool need = __any_sync(0xffffffffu, good && mx > m_ref + RESCALE_THRESHOLD);
+      float* my_slot = mine + (j & 1) * 33;
+      float* their_slot = theirs + (j & 1) * 33;
+      my_slot[lane] = mx;
+      if (lane == 0) my_slot[32] = __int_as_float((need ? 1 : 0) | (good ? 0 : 2));
+      pair_sync(bar_id, 64);
+      const int their_flags = __float_as_int(their_slot[32]);
+      const float their_mx = their_slot[lane];
+      if (!good || (their_flags & 2)) { ok = false; break; }
+      if (need || (their_flags & 1)) {
+        // Rare: move the reference of the rows whose max grew too far, then
+        // recompute this tile's P (S is still in TMEM) and rescale O and l.
+        const float row_mx = fmaxf(mx, their_mx);
+        const float m_new = row_mx > m_ref + RESCALE_THRESHOLD ? row_mx : m_ref;
+        const float alpha = ex2(m_ref - m_new);      // 0 while nothing has been accumulated
+        tmem_wait_st();
+        ta = tb = 0;
+        make_p(rows_valid, m_new, ta, tb, nullptr);
+        if (half == 0 && j > 0) {
+#pragma unroll
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(O_ + cc * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(O_ + cc * 32, o);
+          }
+        }
+        la = f2_pack(f2_lo(la) * alpha, f2_hi(la) * alpha);
+        lb = f2_pack(f2_lo(lb) * alpha, f2_hi(lb) * alpha);
+        m_ref = m_new;
+      }
+      la = fadd2(la, ta);
+      lb = fadd2(lb, tb);
       tmem_wait_st();
       tc_fence_before();
+      mbar_arrive(&s_free[qi]);                      // the tensor core may overwrite S now
       mbar_arrive(&p_full[qi]);
     }
-    if (ok && !wait_bar_warp(g, &p_free[qi], (n - 1) & 1, 9)) ok = false;
-    if (ok) {
-      tc_fence_after();
-      float o[HD];
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+    if (n > 0 && qi < nq_tiles) {
+      // Epilogue: combine the two warps' row sums, then each warp normalises
+      // and writes its half of the head dimension.
+      bool good = ok && wait_bar_warp(g, &p_free[qi], (n - 1) & 1, 9);
+      const float l_mine = (f2_lo(la) + f2_hi(la)) + (f2_lo(lb) + f2_hi(lb));
+      float* my_slot = mine + (n & 1) * 33;
+      float* their_slot = theirs + (n & 1) * 33;
+      my_slot[lane] = l_mine;
+      if (lane == 0) my_slot[32] = __int_as_float(good ? 0 : 2);
+      if (ok) pair_sync(bar_id, 64);                 // both warps of a pair left the loop alike
+      if (ok && good && !(__float_as_int(their_slot[32]) & 2)) {
+        const float l = l_mine + their_slot[lane];
+        tc_fence_after();
         uint32_t v[32];
-        tmem_ld32(O_ + c * 32, v);
+        tmem_ld32(O_ + half * 32, v);
         tmem_wait_ld();
         reg_fence(v);
+        const int row = q0 + qi * BM + r;
+        if (row < a.n_q) {
+          const float inv = 1.f / l;
+          float o[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(v[i]);
-      }
-      const int row = q0 + qi * BM + r;
-      if (row < a.n_q) {
-        const float l = f2_lo(l2) + f2_hi(l2);
-        const float inv = 1.f / l;
-        if (a.n_splits == 1) {
-          using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-          T* dst = reinterpret_cast<T*>(a.out) + ((int64_t)row * a.num_heads + h) * HD;
-          store_row<BF16>(dst, o, inv);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + (((int64_t)split * a.n_q + row) * a.num_heads + h) * HD);
+          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * inv;
+          if (a.n_splits == 1) {
+            using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.out) +
+                                                  ((int64_t)row * a.num_heads + h) * HD + half * 32);
 #pragma unroll
-          for (int i = 0; i < HD / 4; ++i)
-            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
-          a.part_lse[((int64_t)split * a.n_q + row) * a.num_heads + h] = m_ref + __log2f(l);
+            for (int i = 0; i < 4; ++i) {
+              uint4 u;
+              u.x = pack2<BF16>(o[8 * i + 0], o[8 * i + 1]);
+              u.y = pack2<BF16>(o[8 * i + 2], o[8 * i + 3]);
+              u.z = pack2<BF16>(o[8 * i + 4], o[8 * i + 5]);
+              u.w = pack2<BF16>(o[8 * i + 6], o[8 * i + 7]);
+              dst[i] = u;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(
+                a.part_o + (((int64_t)split * a.n_q + row) * a.num_heads + h) * HD + half * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            if (half == 0) a.part_lse[((int64_t)split * a.n_q + row) * a.num_heads + h] = m_ref + __log2f(l);
+          }
         }
       }
     }
+    __syncwarp();
+    tmem_wait_ld();                                  // nothing of ours in flight on the way out
+    tmem_wait_st();
   }
   tc_fence_before();
   __syncthreads();
