@@ -189,6 +189,20 @@ def workload(args):
     return w
 
 
+def aggregate(ms, frames, world, device="cpu"):
+    """Whole-job numbers of independent replicas: the slowest rank's time and
+    the frames of all ranks (max and sum over ranks; identity for one rank)."""
+    if world <= 1:
+        return ms, frames
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    f = torch.tensor([float(frames)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(f.item())
+
+
 def run_ours(args, rank, world):
     import torch
     from streaming_paged_kv_gb300 import build
@@ -243,17 +257,13 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, total_frames = aggregate(ev0.elapsed_time(ev1), K, world, dev)
     launches, attn_launches, attn_ms = kvc.kvc_get_counters(st.c.h, reset=True)
     st.c.set_option(kvc.KVC_OPT_TIMING, 0)
     status = kvc.kvc_device_status(st.c.h, st.c._stream())
     if status != 0:
         raise RuntimeError(f"device status {status}")
-    value = world * K / (ms / 1e3)
+    value = total_frames / (ms / 1e3)
     pk = peaks()
     achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
     roofline = {
@@ -332,13 +342,9 @@ def run_e2e(args, kvc, w, dev, rank, world):
     for _ in range(K):
         frame()
     torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+    dt, total_frames = aggregate(time.perf_counter() - t0, K, world, dev)
     c.close()
-    return {"value": world * K / dt, "unit": UNIT, "h2d_bytes_per_step": L * 3 * T * H * D * 2,
+    return {"value": total_frames / dt, "unit": UNIT, "h2d_bytes_per_step": L * 3 * T * H * D * 2,
             "d2h_bytes_per_step": L * T * H * D * 2, "steps": K,
             "frames_timed": [w.n_frames - K, w.n_frames - 1]}
 

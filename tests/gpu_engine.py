@@ -112,3 +112,49 @@ class ParityEngine:
 
     def close(self):
         self.c.close()
+
+
+def _frame_job(args):
+    from streaming_paged_kv_gb300.inputs import frame_qkv
+    return frame_qkv(*args)
+
+
+def make_pool(workers=None):
+    """Process pool for input generation (spawn context: safe next to an
+    initialised CUDA context)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import os
+    n = workers or max(1, min(16, (os.cpu_count() or 2) - 1))
+    return cf.ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn"))
+
+
+class FrameSource:
+    """Seeded frames of one workload, generated by a process pool with a
+    bounded look-ahead (at most `ahead` frames in flight or buffered)."""
+
+    def __init__(self, w, pool, seed=0, ahead=48):
+        self.w, self.pool, self.seed, self.ahead = w, pool, seed, ahead
+        self.head_scale = k_head_scale(seed, w.wid, w.num_heads) if w.k_head_scale else None
+
+    def frames(self, frame_ids, layer):
+        from collections import deque
+        w = self.w
+        ids = iter(frame_ids)
+        pending = deque()
+
+        def submit():
+            for f in ids:
+                pending.append(self.pool.submit(_frame_job, (self.seed, w.wid, f, layer, w.page_size,
+                                                             w.num_heads, w.head_dim, w.dtype,
+                                                             self.head_scale)))
+                return True
+            return False
+
+        for _ in range(self.ahead):
+            if not submit():
+                break
+        while pending:
+            out = pending.popleft().result()
+            submit()
+            yield out
