@@ -198,7 +198,10 @@ enum {
   KVC_OPT_ATTN_KERNEL = 1, /* 0 auto, 1 CUDA-core kernel, 2 tensor-core (tcgen05) kernel */
   KVC_OPT_NUM_SPLITS = 2,  /* 0 auto, else the number of KV splits (<= max_kv_splits)     */
   KVC_OPT_WAIT_BUDGET = 3, /* bounded-wait budget in SM clock cycles; 0 => default (~2 s) */
-  KVC_OPT_TIMING = 4       /* 1: time every attention launch with CUDA events            */
+  KVC_OPT_TIMING = 4,      /* 1: time every attention launch with CUDA events            */
+  KVC_OPT_STALL_TEST = 5   /* test only, 1: the tensor-core kernel first waits on a barrier
+                              that nothing signals, so its bounded wait runs out and the run
+                              reports KVC_ERR_DEVICE_TIMEOUT (no output is written)           */
 };
 int kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
 

@@ -395,7 +395,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
   uint64_t* p_full = bars + 5 + 2 * STAGES;     // [QT] P_i written (and O_i rescaled)
   uint64_t* p_free = bars + 7 + 2 * STAGES;     // [QT] P_i V product done
   uint64_t* drain = bars + 9 + 2 * STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10 + 2 * STAGES);
+  uint64_t* never = bars + 10 + 2 * STAGES;     // signalled by nothing (timeout test)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11 + 2 * STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -422,6 +423,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       mbar_init(&p_free[i], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -495,7 +497,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
         }
         __syncwarp();
       };
-      bool ok = wait_bar_warp(g, q_full, 0, 2) && wait_bar_warp(g, &kv_full[0], 0, 3);
+      // Timeout test: a wait that nothing ends, so the bound runs out and the
+      // whole CTA takes the abort path.
+      bool ok = !a.stall_test || wait_bar_warp(g, never, 0, 12);
+      ok = ok && wait_bar_warp(g, q_full, 0, 2) && wait_bar_warp(g, &kv_full[0], 0, 3);
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < nq_tiles; ++i) issue_s(i, 0);

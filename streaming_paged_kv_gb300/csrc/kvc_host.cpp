@@ -158,6 +158,7 @@ struct kvc_handle {
   int opt_splits = 0;
   long long wait_budget = 0;
   bool timing = false;
+  int stall_test = 0;
   // Counters.
   int64_t launches = 0, attn_launches = 0;
   double attn_ms = 0.0;
@@ -505,6 +506,7 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
   a.n_splits = splits;
   a.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
   a.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
+  a.stall_test = h->stall_test;
   cudaStream_t st = (cudaStream_t)stream;
   if (h->timing) record_timing(h, 0, st);
   cudaError_t err = kernel == 2 ? kvc::launch_attn_tc(a, h->maps, block, h->g.max_pages, h->cfg.dtype, st)
@@ -618,6 +620,10 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
     case KVC_OPT_WAIT_BUDGET:
       if (value < 0) return KVC_ERR_INVALID_ARG;
       h->wait_budget = value;
+      return KVC_OK;
+    case KVC_OPT_STALL_TEST:
+      if (value < 0 || value > 1) return KVC_ERR_INVALID_ARG;
+      h->stall_test = (int)value;
       return KVC_OK;
     case KVC_OPT_TIMING:
       if (value && !h->ev) {

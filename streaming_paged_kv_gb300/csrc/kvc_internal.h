@@ -68,6 +68,7 @@ struct AttnArgs {
   int32_t n_splits;
   float sm_scale_log2;    // sm_scale * log2(e)
   long long wait_budget;  // clock cycles per bounded wait
+  int32_t stall_test;     // 1: wait once on a barrier nothing signals (timeout test)
 };
 
 // kvc_kernels.cu

@@ -170,6 +170,7 @@ extern "C" int kvc_paged_attention_static(const void* cache_block, int32_t dtype
   const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt((float)head_dim);
   a.sm_scale_log2 = scale * 1.4426950408889634f;
   a.wait_budget = 4000000000LL;
+  a.stall_test = 0;
   if (launch_attn_simt(a, dtype, st) != cudaSuccess) return KVC_ERR_CUDA;
   if (splits > 1 && launch_merge(a, dtype, st) != cudaSuccess) return KVC_ERR_CUDA;
   return KVC_OK;

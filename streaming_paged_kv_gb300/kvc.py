@@ -27,7 +27,7 @@ ERRORS = {
     -4: "NOTHING_TO_ROLLBACK", -5: "ROLLBACK_AFTER_EVICT", -6: "NO_PLAN", -7: "STALE_PLAN",
     -8: "CUDA", -9: "DEVICE_TIMEOUT", -10: "EMPTY", -11: "NO_DEVICE", -12: "TOO_LARGE",
 }
-KVC_OPT_ATTN_KERNEL, KVC_OPT_NUM_SPLITS, KVC_OPT_WAIT_BUDGET, KVC_OPT_TIMING = 1, 2, 3, 4
+KVC_OPT_ATTN_KERNEL, KVC_OPT_NUM_SPLITS, KVC_OPT_WAIT_BUDGET, KVC_OPT_TIMING, KVC_OPT_STALL_TEST = 1, 2, 3, 4, 5
 
 
 class kvc_config(ctypes.Structure):

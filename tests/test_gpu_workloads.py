@@ -126,10 +126,11 @@ def test_s224_full_stream(kvc, pool):
 
 
 def test_bounded_wait_reports_timeout_and_recovers(kvc):
-    """A wait budget of one cycle makes the tensor-core kernel's first
-    mbarrier wait run out: the kernel records the timeout, drains, frees TMEM
-    and returns; the host sees KVC_ERR_DEVICE_TIMEOUT and the next run with
-    the normal budget is correct."""
+    """The tensor-core kernel's MMA warp waits on a barrier nothing signals
+    (KVC_OPT_STALL_TEST) with a short budget: the wait runs out, the kernel
+    records the timeout, every role drains, TMEM is freed and the kernel
+    returns; the host sees KVC_ERR_DEVICE_TIMEOUT, and the next run with the
+    normal settings is correct (the context is still usable)."""
     from streaming_paged_kv_gb300.inputs import frame_qkv
     c = kvc.PagedKVCache(1, 4, 64, 256, "bf16", 2, 4, 2, 64)
     try:
@@ -147,9 +148,12 @@ def test_bounded_wait_reports_timeout_and_recovers(kvc):
     c.plan()
     qd = q.cuda()
     out = torch.empty_like(qd)
-    c.set_option(kvc.KVC_OPT_WAIT_BUDGET, 1)
+    c.set_option(kvc.KVC_OPT_WAIT_BUDGET, 2_000_000)    # about a millisecond
+    c.set_option(kvc.KVC_OPT_STALL_TEST, 1)
     c.run(0, qd, out)
     assert kvc.kvc_device_status(c.h, c._stream()) == -9
+    assert kvc.kvc_device_status(c.h, c._stream()) == 0    # reading clears the status
+    c.set_option(kvc.KVC_OPT_STALL_TEST, 0)
     c.set_option(kvc.KVC_OPT_WAIT_BUDGET, 0)
     c.run(0, qd, out)
     assert kvc.kvc_device_status(c.h, c._stream()) == 0
