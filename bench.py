@@ -179,6 +179,26 @@ class Stream:
         return self.w.page_size * (s["scale_pages"] + s["live_pages"]) + s["special_tokens"]
 
 
+def profiled_traffic(alg_bytes_per_launch):
+    """DRAM bytes per attention launch from the committed ncu summary, scaled to
+    this run's average launch by algorithmic bytes -- or None when the kernel
+    source differs from the one the counters were taken on."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", "attn_tc_s518_l1f200_full.md")
+    src = os.path.join(ROOT, "streaming_paged_kv_gb300", "csrc", "kvc_attn_tc.cu")
+    try:
+        text = open(prof, encoding="utf-8").read()
+        sha = re.search(r"^kernel_source_sha256: ([0-9a-f]+)$", text, re.M).group(1)
+        dram = float(re.search(r"^dram_bytes_per_launch: (\d+)$", text, re.M).group(1))
+        alg = float(re.search(r"^alg_bytes_per_launch: (\d+)$", text, re.M).group(1))
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() != sha:
+            return None
+        return dram * alg_bytes_per_launch / alg
+    except Exception:
+        return None
+
+
 def workload(args):
     from streaming_paged_kv_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
@@ -269,7 +289,7 @@ def run_ours(args, rank, world):
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None,
-        "traffic": None,
+        "traffic": profiled_traffic(bytes_alg / max(attn_launches, 1)),
         "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
         "kernel": "paged attention (kvc_run attention launch)",
         "flops_per_launch": flops / max(attn_launches, 1),
