@@ -17,23 +17,26 @@
 //
 // CTA = two 128-row query tiles (Q0, Q1) x one head x one KV split; each K/V
 // tile is loaded once and serves both query tiles.  Warps:
-//   0-7   softmax + epilogue of Q0, 8-15 softmax + epilogue of Q1.  Within a
-//         query tile, warp w owns TMEM lanes [32(w%4), +32) (query rows) and
-//         columns [64 h, +64) of each S tile, h = (w/4)%2: two warps share
-//         every row, each holding half of its scores
-//   16    TMA producer (one lane): Q0/Q1, then K/V tiles into a 4-stage ring
-//   17    MMA issuer (one lane): S_i = Q_i K^T into TMEM, O_i += P_i V with P_i
-//         read from TMEM
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
-// P0 [384,448) P1 [448,512); P holds two 16-bit values per column.
+//   0-3   softmax + epilogue of Q0, 4-7 softmax + epilogue of Q1: one thread
+//         per query row (warp w owns TMEM lanes [32(w%4), +32)), holding the
+//         row's 128 scores of a tile in registers
+//   8     TMA producer (one lane): Q0/Q1, then K/V tiles into a 5-stage ring
+//   9     P V issuer (one lane): O_i += P V with P read from TMEM
+//   10    S issuer (one lane): S = Q_i K^T into TMEM
+// Score tiles are numbered in issue order k = j * nq + i (KV tile j, query
+// tile i) and rotate through three 128-column TMEM buffers, b = k mod 3.  A
+// softmax thread reads its whole row of S(k), writes P(k) as 16-bit pairs over
+// the first 64 columns of the same buffer, and the P V product reads it there.
+// S(k+3) may enter buffer b once P(k) V has completed, so while one query
+// tile's warps exponentiate, the other tile's next scores are already being
+// computed.  TMEM (512 columns): buffers [0,128) [128,256) [256,384),
+// O0 [384,448), O1 [448,512).
 // Q and K/V tiles use the 128-byte swizzle that both TMA and the tensor core
 // understand.  Scores live in the log2 domain (scaled by sm_scale * log2 e).
-// Each warp exponentiates its half of the row against the running reference
-// max m_ref of the row.  The reference moves only when a score exceeds it by
-// more than 8 (a factor 256): then the two warps of the row agree on the new
-// reference through shared memory, recompute that tile's P from S and rescale
-// O and the row sums.  Otherwise P is taken against the stale reference, which
-// fp32 accumulation absorbs.
+// Each row keeps a reference max m_ref; a tile whose row max exceeds it by
+// more than 8 (a factor 256) moves it to that max, and O and the row sum are
+// rescaled (O only after the previous P V product has completed).  Otherwise
+// P is taken against the stale reference, so every P value is at most 2^8.
 //
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
 // the fact in the status word, raises a CTA-wide abort flag, and every role
@@ -65,16 +68,22 @@ constexpr int BM = 128;           // query rows per query tile
 constexpr int QT = 2;             // query tiles per CTA
 constexpr int BN = 128;           // KV rows per tile
 constexpr int HD = 64;            // head dim of this kernel
-constexpr int STAGES = 4;
-constexpr int NUM_THREADS = 576;
-constexpr int PRODUCER_WARP = 16, MMA_WARP = 17;
-constexpr int SOFTMAX_THREADS = 2 * BM;              // per query tile: two warps per row
+constexpr int STAGES = 5;         // K/V ring depth
+constexpr int NBUF = 3;           // rotating S / P buffers in TMEM
+constexpr int NUM_THREADS = 352;
+// Register budget: the register file is split over the four SM sub-partitions
+// and warp w runs on sub-partition w % 4, so with eleven warps three
+// sub-partitions hold three warps each: 16384 / (3 * 32) = 170, rounded down
+// to 168.
+constexpr int REG_BOUND_THREADS = 384;
+constexpr int PRODUCER_WARP = 8, PV_WARP = 9, S_WARP = 10;
+constexpr int GROUP_THREADS = BM;                    // softmax threads per query tile
 constexpr uint32_t TILE_BYTES = BN * HD * 2;         // 16 KB: one K or V tile
 constexpr uint32_t Q_BYTES = BM * HD * 2;            // 16 KB per query tile
 constexpr uint32_t TMEM_COLS = 512;
-__host__ __device__ constexpr uint32_t s_col(int i) { return i * BN; }
-__host__ __device__ constexpr uint32_t o_col(int i) { return 2 * BN + i * HD; }
-__host__ __device__ constexpr uint32_t p_col(int i) { return 2 * BN + 2 * HD + i * (BN / 2); }
+__host__ __device__ constexpr uint32_t buf_col(int b) { return b * BN; }
+__host__ __device__ constexpr uint32_t o_col(int i) { return NBUF * BN + i * HD; }
+static_assert(o_col(QT) <= TMEM_COLS, "TMEM budget");
 constexpr float RESCALE_THRESHOLD = 8.0f;            // log2 units
 constexpr long long kDrainBudget = 1LL << 26;        // cycles for draining after an abort
 
@@ -83,10 +92,7 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
 constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + STAGES * TILE_BYTES;
-// Row exchange between the two warps of a row: [pair][warp half][slot][33 floats].
-constexpr uint32_t OFF_XCH = OFF_BAR + 256;
-constexpr uint32_t XCH_BYTES = 8 * 2 * 2 * 33 * 4;
-constexpr uint32_t SMEM_BYTES = OFF_XCH + XCH_BYTES + 1024;  // + alignment slack
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
 
 // ------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -197,11 +203,6 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// Named barrier over `count` threads (the two warps of a row pair).
-__device__ __forceinline__ void pair_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
 // start>>4 in [0,14), LBO>>4 in [16,30), SBO>>4 in [32,46), version 1 at 46,
 // swizzle mode 2 = 128B at [61,64)).
@@ -262,17 +263,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
       "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
       "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr)
       : "memory");
 }
 
@@ -351,34 +341,16 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   return r;
 }
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t scale_pair(uint32_t packed, float alpha) {
-  if constexpr (BF16) {
-    __nv_bfloat162 t = *reinterpret_cast<__nv_bfloat162*>(&packed);
-    return pack2<true>(__low2float(t) * alpha, __high2float(t) * alpha);
-  } else {
-    __half2 t = *reinterpret_cast<__half2*>(&packed);
-    return pack2<false>(__low2float(t) * alpha, __high2float(t) * alpha);
-  }
-}
-
-template <bool BF16>
-__device__ __forceinline__ void store_row(void* dst, const float* o, float inv) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) {
-    uint4 u;
-    u.x = pack2<BF16>(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
-    u.y = pack2<BF16>(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
-    u.z = pack2<BF16>(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
-    u.w = pack2<BF16>(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
-    d[i] = u;
-  }
-}
-
 // ------------------------------------------------------------------ kernel
+// 32 consecutive TMEM columns of this thread's lane into v[off, off + 32).
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&v)[N]) {
+  static_assert(OFF + 32 <= N, "range");
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[OFF]));
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(REG_BOUND_THREADS, 1)
 attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
                const __grid_constant__ CUtensorMap q_map, int32_t page_base) {
   extern __shared__ uint8_t smem_raw[];
@@ -388,41 +360,49 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
   uint8_t* sV = smem + OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;                 // [STAGES]
-  uint64_t* kv_empty = bars + 1 + STAGES;       // [STAGES]
-  uint64_t* s_full = bars + 1 + 2 * STAGES;     // [QT] S_i written by the tensor core
-  uint64_t* s_free = bars + 3 + 2 * STAGES;     // [QT] S_i copied out by its warpgroup
-  uint64_t* p_full = bars + 5 + 2 * STAGES;     // [QT] P_i written (and O_i rescaled)
-  uint64_t* p_free = bars + 7 + 2 * STAGES;     // [QT] P_i V product done
-  uint64_t* drain = bars + 9 + 2 * STAGES;
-  uint64_t* never = bars + 10 + 2 * STAGES;     // signalled by nothing (timeout test)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11 + 2 * STAGES);
+  uint64_t* kv_full = bars + 1;                   // [STAGES]
+  uint64_t* kv_empty = kv_full + STAGES;          // [STAGES]
+  uint64_t* s_full = kv_empty + STAGES;           // [NBUF] S(k) written by the tensor core
+  uint64_t* p_full = s_full + NBUF;               // [NBUF] P(k) written (and O rescaled)
+  uint64_t* buf_free = p_full + NBUF;             // [NBUF] P(k) V done: the buffer may take S(k+3)
+  // [QT][2] O_i += P_i(j) V(j) done, on barrier [i][j % 2].  Alternating
+  // barriers keep every parity wait unambiguous: when a softmax thread of
+  // tile j waits for P_i(j-1) V, the product of tile j-3 has already
+  // completed and that of tile j+1 has not been issued, so the barrier it
+  // polls is either one phase short of the target or at it.
+  uint64_t* o_done = buf_free + NBUF;
+  uint64_t* drain = o_done + 2 * QT;               // [2] one per MMA-issuing warp
+  uint64_t* never = drain + 2;                    // signalled by nothing (timeout test)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  static_assert((1 + 2 * STAGES + 3 * NBUF + 2 * QT + 3) * 8 + 8 <= 256, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y, split = blockIdx.z;
   const int q0 = blockIdx.x * (QT * BM);
   const bool has_q1 = q0 + BM < a.n_q;
-  const int nq_tiles = has_q1 ? 2 : 1;
+  const int nq = has_q1 ? 2 : 1;
   const int t0 = (int)(((int64_t)split * a.n_tiles) / a.n_splits);
   const int t1 = (int)(((int64_t)(split + 1) * a.n_tiles) / a.n_splits);
   const int n = t1 - t0;
+  const int n_s = n * nq;                         // score tiles of this CTA
   Guard g{abort_flag, a.status, a.wait_budget};
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], 2);                 // the S and the P V issuer
     }
-    for (int i = 0; i < QT; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], SOFTMAX_THREADS);
-      mbar_init(&p_full[i], SOFTMAX_THREADS);
-      mbar_init(&p_free[i], 1);
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], GROUP_THREADS);
+      mbar_init(&buf_free[b], 1);
     }
-    mbar_init(drain, 1);
+    for (int i = 0; i < 2 * QT; ++i) mbar_init(&o_done[i], 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(never, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -446,7 +426,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       const bool leader = elect_one();
       int issued = 0;
       if (leader) {
-        mbar_expect_tx(q_full, nq_tiles * Q_BYTES);
+        mbar_expect_tx(q_full, nq * Q_BYTES);
         tma_load_2d(sQ, &q_map, h * HD, q0, q_full);
         if (has_q1) tma_load_2d(sQ + Q_BYTES, &q_map, h * HD, q0 + BM, q_full);
       }
@@ -469,229 +449,230 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
           drain_bar(&kv_full[j % STAGES], (j / STAGES) & 1);
       }
     }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop and its waits with warp-uniform values;
-    // one elected lane issues the MMAs and the commits.
+  } else if (warp == S_WARP || warp == PV_WARP) {
+    // ------------------------------------------------------ MMA issuers
+    // Two warps feed the tensor core: one issues the S MMAs, the other the
+    // P V MMAs, so that each one's barrier waits overlap the other's issue.
+    // Each runs its loop and waits with the whole warp (warp-uniform values);
+    // one elected lane issues the MMAs and the commits.  Indices and barrier
+    // phases advance incrementally.
     if (n > 0) {
       const bool leader = elect_one();
-      constexpr uint32_t IDESC_S = idesc_f16(BM, BN, BF16, false);
-      constexpr uint32_t IDESC_O = idesc_f16(BM, HD, BF16, true);
       // Descriptors are built once; a step along K or to another stage only
       // adds to the start-address field (address >> 4, 14 bits, no carry for
       // shared-memory addresses below 256 KB), so each MMA costs one add.
-      const uint64_t dQ[QT] = {sdesc_sw128(smem_u32(sQ), 16, 1024), sdesc_sw128(smem_u32(sQ) + Q_BYTES, 16, 1024)};
-      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
       constexpr uint64_t STAGE_STEP = TILE_BYTES >> 4;     // next K/V stage
       constexpr uint64_t K16_STEP = 32 >> 4;               // 16 bf16 along K inside a 128-byte row
       constexpr uint64_t V16_STEP = (16 * 128) >> 4;       // 16 rows of V
-      auto issue_s = [&](int i, int j) {
-        const uint64_t dK = dK0 + (uint64_t)(j % STAGES) * STAGE_STEP;
-        const uint32_t d = tmem + s_col(i);
-        if (leader) {
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k)
-            umma(d, dQ[i] + k * K16_STEP, dK + k * K16_STEP, IDESC_S, k > 0);
-          umma_commit(&s_full[i]);
-        }
-        __syncwarp();
-      };
-      // Timeout test: a wait that nothing ends, so the bound runs out and the
-      // whole CTA takes the abort path.
-      bool ok = !a.stall_test || wait_bar_warp(g, never, 0, 12);
-      ok = ok && wait_bar_warp(g, q_full, 0, 2) && wait_bar_warp(g, &kv_full[0], 0, 3);
-      if (ok) {
-        tc_fence_after();
-        for (int i = 0; i < nq_tiles; ++i) issue_s(i, 0);
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        const int st = j % STAGES;
-        if (j + 1 < n) ok = wait_bar_warp(g, &kv_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1, 3);
-        // Per query tile: its next S as soon as its warps have copied S out,
-        // then its P V product once P is in TMEM.
-        for (int i = 0; ok && i < nq_tiles; ++i) {
-          if (j + 1 < n) {
-            ok = wait_bar_warp(g, &s_free[i], j & 1, 4);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(i, j + 1);
+      constexpr uint64_t Q_STEP = Q_BYTES >> 4;            // second query tile
+      int i = 0, b = 0, st = 0;
+      uint32_t kv_par = 0, buf_par = 0;                    // one parity bit per stage / buffer
+      bool ok = true;
+      if (warp == S_WARP) {
+        // S(k) = Q_i K(j)^T into buffer k mod 3, once K(j) has landed and the
+        // P V product that last read the buffer has completed.
+        constexpr uint32_t IDESC_S = idesc_f16(BM, BN, BF16, false);
+        const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+        ok = wait_bar_warp(g, q_full, 0, 2);
+        for (int k = 0; ok && k < n_s; ++k) {
+          if (i == 0) {
+            ok = wait_bar_warp(g, &kv_full[st], (kv_par >> st) & 1, 3);
+            kv_par ^= 1u << st;
           }
-          ok = wait_bar_warp(g, &p_full[i], j & 1, 5);
+          if (ok && k >= NBUF) {
+            ok = wait_bar_warp(g, &buf_free[b], (buf_par >> b) & 1, 4);
+            buf_par ^= 1u << b;
+          }
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dK = dK0 + (uint64_t)st * STAGE_STEP;
+          const uint64_t dQ = dQ0 + (uint64_t)i * Q_STEP;
+          const uint32_t d = tmem + buf_col(b);
+          if (leader) {
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk)
+              umma(d, dQ + kk * K16_STEP, dK + kk * K16_STEP, IDESC_S, kk > 0);
+            umma_commit(&s_full[b]);
+            if (i == nq - 1) umma_commit(&kv_empty[st]);
+          }
+          __syncwarp();
+          b = b == NBUF - 1 ? 0 : b + 1;
+          if (++i == nq) {
+            i = 0;
+            st = st == STAGES - 1 ? 0 : st + 1;
+          }
+        }
+      } else {
+        // O_i += P(k) V(j), P read from the first 64 columns of buffer k mod 3.
+        // Timeout test: a wait that nothing ends, so the bound runs out and the
+        // whole CTA takes the abort path.
+        constexpr uint32_t IDESC_O = idesc_f16(BM, HD, BF16, true);
+        const uint64_t dV0 = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
+        uint32_t p_par = 0;
+        ok = !a.stall_test || wait_bar_warp(g, never, 0, 12);
+        for (int k = 0, j = 0; ok && k < n_s; ++k) {
+          if (i == 0) {
+            // V(j) landed (already true in practice: S(k) needed K(j) of the same copy).
+            ok = wait_bar_warp(g, &kv_full[st], (kv_par >> st) & 1, 3);
+            kv_par ^= 1u << st;
+          }
+          if (ok) {
+            ok = wait_bar_warp(g, &p_full[b], (p_par >> b) & 1, 5);
+            p_par ^= 1u << b;
+          }
           if (!ok) break;
           tc_fence_after();
           const uint64_t dV = dV0 + (uint64_t)st * STAGE_STEP;
-          const uint32_t o = tmem + o_col(i), pa = tmem + p_col(i);
+          const uint32_t o = tmem + o_col(i), pa = tmem + buf_col(b);
           if (leader) {
 #pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-              umma_ts(o, pa + k * 8, dV + k * V16_STEP, IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
-            umma_commit(&p_free[i]);
+            for (int kk = 0; kk < BN / 16; ++kk)
+              umma_ts(o, pa + kk * 8, dV + kk * V16_STEP, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&buf_free[b]);
+            umma_commit(&o_done[2 * i + (j & 1)]);
+            if (i == nq - 1) umma_commit(&kv_empty[st]);
           }
           __syncwarp();
+          b = b == NBUF - 1 ? 0 : b + 1;
+          if (++i == nq) {
+            i = 0;
+            ++j;
+            st = st == STAGES - 1 ? 0 : st + 1;
+          }
         }
-        if (ok && leader) umma_commit(&kv_empty[st]);
-        __syncwarp();
       }
-      // Every MMA this warp issued has completed once `drain` flips.
+      // Every MMA this warp issued has completed once its drain barrier flips.
+      uint64_t* my_drain = warp == S_WARP ? drain : drain + 1;
       if (leader) {
-        umma_commit(drain);
-        drain_bar(drain, 0);
+        umma_commit(my_drain);
+        drain_bar(my_drain, 0);
       }
       __syncwarp();
     }
   } else {
     // ------------------------------------------------ softmax + epilogue
-    const int qi = warp >> 3;                        // query tile of this warp
-    const int half = (warp >> 2) & 1;                // which 64 columns of each S tile
+    const int qi = warp >> 2;                        // query tile of this warp
     const int quarter = warp & 3;                    // TMEM lanes [32 quarter, +32)
-    const int pair = qi * 4 + quarter;               // the two warps sharing these rows
     const int r = quarter * 32 + lane;               // query row within the tile == TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t S_ = lane_base + s_col(qi) + half * 64;
-    const uint32_t P_ = lane_base + p_col(qi) + half * 32;
     const uint32_t O_ = lane_base + o_col(qi);
-    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);
-    float* mine = xch + (pair * 2 + half) * 66;      // two slots of 33
-    float* theirs = xch + (pair * 2 + (half ^ 1)) * 66;
-    const int bar_id = 1 + pair;
-    const int col0 = half * 64;
     const float sl2 = a.sm_scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     float m_ref = -INFINITY;
-    uint64_t la = 0, lb = 0;                         // row-sum partials over this warp's columns
-    bool ok = n > 0 && qi < nq_tiles;                // the same for both warps of a pair
-
-    // P for this warp's 64 columns of tile S into TMEM, against reference m:
-    // returns the partial sums; clamps the exponent so that a stale reference
-    // can never produce inf (such tiles are recomputed).
-    auto make_p = [&](int rows_valid, float m, uint64_t& ta, uint64_t& tb, float* smax) {
-      const uint64_t negx2 = f2_pack(-m, -m);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        uint32_t v[32];
-        tmem_ld32(S_ + u * 32, v);
-        tmem_wait_ld();
-        reg_fence(v);
-        if (rows_valid < col0 + 64) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (col0 + u * 32 + i >= rows_valid) v[i] = __float_as_uint(-INFINITY);
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float s0 = __uint_as_float(v[2 * i]), s1 = __uint_as_float(v[2 * i + 1]);
-          if (smax) *smax = fmax3(*smax, s0, s1);
-          const uint64_t x = ffma2(f2_pack(s0, s1), sl2x2, negx2);
-          const float p0 = ex2(fminf(f2_lo(x), 120.f)), p1 = ex2(fminf(f2_hi(x), 120.f));
-          if (i & 1) tb = fadd2(tb, f2_pack(p0, p1));
-          else ta = fadd2(ta, f2_pack(p0, p1));
-          pk[i] = pack2<BF16>(p0, p1);
-        }
-        tmem_st16(P_ + u * 16, pk);
-      }
-    };
+    uint64_t la = 0, lb = 0;                         // row-sum partials (two fp32 pairs)
+    bool ok = n > 0 && qi < nq;                      // warp-uniform
 
     int rows_next = ok ? a.tiles[t0].rows : 0;
     for (int j = 0; ok && j < n; ++j) {
+      const int k = j * nq + qi, b = k % NBUF;
       const int rows_valid = rows_next;
       if (j + 1 < n) rows_next = a.tiles[t0 + j + 1].rows;   // prefetch for the next tile
-      bool good = wait_bar_warp(g, &s_full[qi], j & 1, 6);
-      // P_i is free (and O_i stable) once the P V product of the previous tile has completed.
-      if (good && j > 0) good = wait_bar_warp(g, &p_free[qi], (j - 1) & 1, 8);
+      ok = wait_bar_warp(g, &s_full[b], (k / NBUF) & 1, 6);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t S_ = lane_base + buf_col(b);
+      uint32_t v[BN];
+      tmem_ld32_at<0>(S_, v);
+      tmem_ld32_at<32>(S_ + 32, v);
+      tmem_ld32_at<64>(S_ + 64, v);
+      tmem_ld32_at<96>(S_ + 96, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
+      if (rows_valid < BN) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= rows_valid) v[c] = __float_as_uint(-INFINITY);
+      }
+      // Row max of the tile (four independent chains), in log2 units.
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN; c += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          m4[u] = fmax3(m4[u], __uint_as_float(v[c + 2 * u]), __uint_as_float(v[c + 2 * u + 1]));
+      }
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+      const bool moved = mt > m_ref + RESCALE_THRESHOLD;
+      const float m_use = moved ? mt : m_ref;
+      const float alpha = moved ? ex2(m_ref - m_use) : 1.f;   // 0 while nothing has been accumulated
+      // P = 2^(s * scale - m_use) <= 2^8, packed in pairs over S's first 64 columns.
+      const uint64_t negm2 = f2_pack(-m_use, -m_use);
       uint64_t ta = 0, tb = 0;
-      float smax = -INFINITY;
-      if (good) {
-        tc_fence_after();
-        make_p(rows_valid, m_ref, ta, tb, &smax);
-      }
-      // Tell the other warp of these rows whether the reference has to move
-      // (or whether this warp gave up), and this row's score max.
-      const float mx = smax * sl2;
-      const bool need = __any_sync(0xffffffffu, good && mx > m_ref + RESCALE_THRESHOLD);
-      float* my_slot = mine + (j & 1) * 33;
-      float* their_slot = theirs + (j & 1) * 33;
-      my_slot[lane] = mx;
-      if (lane == 0) my_slot[32] = __int_as_float((need ? 1 : 0) | (good ? 0 : 2));
-      pair_sync(bar_id, 64);
-      const int their_flags = __float_as_int(their_slot[32]);
-      const float their_mx = their_slot[lane];
-      if (!good || (their_flags & 2)) { ok = false; break; }
-      if (need || (their_flags & 1)) {
-        // Rare: move the reference of the rows whose max grew too far, then
-        // recompute this tile's P (S is still in TMEM) and rescale O and l.
-        const float row_mx = fmaxf(mx, their_mx);
-        const float m_new = row_mx > m_ref + RESCALE_THRESHOLD ? row_mx : m_ref;
-        const float alpha = ex2(m_ref - m_new);      // 0 while nothing has been accumulated
-        tmem_wait_st();
-        ta = tb = 0;
-        make_p(rows_valid, m_new, ta, tb, nullptr);
-        if (half == 0 && j > 0) {
 #pragma unroll
-          for (int cc = 0; cc < HD / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(O_ + cc * 32, o);
-            tmem_wait_ld();
-            reg_fence(o);
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(O_ + cc * 32, o);
-          }
+        for (int t = 0; t < 16; ++t) {
+          const int e = c * 32 + 2 * t;
+          const uint64_t x = ffma2(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm2);
+          const float p0 = ex2(f2_lo(x)), p1 = ex2(f2_hi(x));
+          if (t & 1) tb = fadd2(tb, f2_pack(p0, p1));
+          else ta = fadd2(ta, f2_pack(p0, p1));
+          pk[t] = pack2<BF16>(p0, p1);
         }
-        la = f2_pack(f2_lo(la) * alpha, f2_hi(la) * alpha);
-        lb = f2_pack(f2_lo(lb) * alpha, f2_hi(lb) * alpha);
-        m_ref = m_new;
+        tmem_st16(S_ + c * 16, pk);
       }
-      la = fadd2(la, ta);
-      lb = fadd2(lb, tb);
+      if (__any_sync(0xffffffffu, moved) && j > 0) {
+        // Rare: rescale O once the previous P V product into it has completed.
+        ok = wait_bar_warp(g, &o_done[2 * qi + ((j - 1) & 1)], ((j - 1) >> 1) & 1, 8);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(O_ + cc * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+          tmem_st32(O_ + cc * 32, o);
+        }
+      }
+      const uint64_t alpha2 = f2_pack(alpha, alpha);
+      la = ffma2(la, alpha2, ta);
+      lb = ffma2(lb, alpha2, tb);
+      m_ref = m_use;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&s_free[qi]);                      // the tensor core may overwrite S now
-      mbar_arrive(&p_full[qi]);
+      mbar_arrive(&p_full[b]);                       // P(k) is in TMEM (and O_i rescaled)
     }
-    if (n > 0 && qi < nq_tiles) {
-      // Epilogue: combine the two warps' row sums, then each warp normalises
-      // and writes its half of the head dimension.
-      bool good = ok && wait_bar_warp(g, &p_free[qi], (n - 1) & 1, 9);
-      const float l_mine = (f2_lo(la) + f2_hi(la)) + (f2_lo(lb) + f2_hi(lb));
-      float* my_slot = mine + (n & 1) * 33;
-      float* their_slot = theirs + (n & 1) * 33;
-      my_slot[lane] = l_mine;
-      if (lane == 0) my_slot[32] = __int_as_float(good ? 0 : 2);
-      if (ok) pair_sync(bar_id, 64);                 // both warps of a pair left the loop alike
-      if (ok && good && !(__float_as_int(their_slot[32]) & 2)) {
-        const float l = l_mine + their_slot[lane];
+    if (n > 0 && qi < nq) {
+      // Epilogue: wait for the last P V product, normalise, write the row.
+      const bool good = ok && wait_bar_warp(g, &o_done[2 * qi + ((n - 1) & 1)], ((n - 1) >> 1) & 1, 9);
+      if (good) {
+        const float l = (f2_lo(la) + f2_hi(la)) + (f2_lo(lb) + f2_hi(lb));
         tc_fence_after();
-        uint32_t v[32];
-        tmem_ld32(O_ + half * 32, v);
+        uint32_t v[HD];
+        tmem_ld32_at<0>(O_, v);
+        tmem_ld32_at<32>(O_ + 32, v);
         tmem_wait_ld();
-        reg_fence(v);
+#pragma unroll
+        for (int c = 0; c < HD; ++c) asm volatile("" : "+r"(v[c])::"memory");
         const int row = q0 + qi * BM + r;
         if (row < a.n_q) {
           const float inv = 1.f / l;
-          float o[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * inv;
           if (a.n_splits == 1) {
             using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.out) +
-                                                  ((int64_t)row * a.num_heads + h) * HD + half * 32);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.out) + ((int64_t)row * a.num_heads + h) * HD);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < HD / 8; ++i) {
+              const float* o = reinterpret_cast<const float*>(&v[8 * i]);
               uint4 u;
-              u.x = pack2<BF16>(o[8 * i + 0], o[8 * i + 1]);
-              u.y = pack2<BF16>(o[8 * i + 2], o[8 * i + 3]);
-              u.z = pack2<BF16>(o[8 * i + 4], o[8 * i + 5]);
-              u.w = pack2<BF16>(o[8 * i + 6], o[8 * i + 7]);
+              u.x = pack2<BF16>(o[0] * inv, o[1] * inv);
+              u.y = pack2<BF16>(o[2] * inv, o[3] * inv);
+              u.z = pack2<BF16>(o[4] * inv, o[5] * inv);
+              u.w = pack2<BF16>(o[6] * inv, o[7] * inv);
               dst[i] = u;
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(
-                a.part_o + (((int64_t)split * a.n_q + row) * a.num_heads + h) * HD + half * 32);
+            float4* dst = reinterpret_cast<float4*>(a.part_o + (((int64_t)split * a.n_q + row) * a.num_heads + h) * HD);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-            if (half == 0) a.part_lse[((int64_t)split * a.n_q + row) * a.num_heads + h] = m_ref + __log2f(l);
+            for (int i = 0; i < HD / 4; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
+                                   __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
+            a.part_lse[((int64_t)split * a.n_q + row) * a.num_heads + h] = m_ref + __log2f(l);
           }
         }
       }
