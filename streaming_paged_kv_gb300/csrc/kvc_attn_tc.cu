@@ -275,6 +275,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1};" ::"r"(taddr), "r"(v)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -572,6 +581,16 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       if (!ok) break;
       tc_fence_after();
       const uint32_t S_ = lane_base + buf_col(b);
+      if (rows_valid < BN) {
+        // Rows of the tile past its valid count never enter the softmax: their
+        // scores are overwritten with -inf in TMEM before the row is read
+        // (a short loop keeps this rare case out of the unrolled hot path).
+        const uint32_t ninf = __float_as_uint(-INFINITY);
+        int c = rows_valid;
+        for (; (c & 7) != 0; ++c) tmem_st1(S_ + c, ninf);
+        for (; c < BN; c += 8) tmem_st8(S_ + c, ninf);
+        tmem_wait_st();
+      }
       uint32_t v[BN];
       tmem_ld32_at<0>(S_, v);
       tmem_ld32_at<32>(S_ + 32, v);
@@ -580,11 +599,6 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
-      if (rows_valid < BN) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= rows_valid) v[c] = __float_as_uint(-INFINITY);
-      }
       // Row max of the tile (four independent chains), in log2 units.
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -619,7 +633,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
         ok = wait_bar_warp(g, &o_done[2 * qi + ((j - 1) & 1)], ((j - 1) >> 1) & 1, 8);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < HD / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(O_ + cc * 32, o);
