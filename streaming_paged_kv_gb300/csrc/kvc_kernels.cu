@@ -191,33 +191,44 @@ attn_simt_kernel(const AttnArgs a) {
 }
 
 // -------------------------------------------------------------- LSE merge
-// out = sum_s 2^(lse_s - lse) O_s with lse = log2 sum_s 2^lse_s; one warp per
-// (query row, head).
+// out = sum_s 2^(lse_s - lse) O_s with lse = log2 sum_s 2^lse_s
+// ([KVC] "Kernel-Level Execution Flow": the split-KV partials of one query row
+// and head combined by their log-sum-exp).  D / 4 threads per (query row, head),
+// one float4 of the head dimension each, so a (row, head) is one contiguous
+// 4 D-byte read per split; the split loop is unrolled to keep several splits'
+// loads in flight.
 template <typename T, int D>
 __global__ void merge_kernel(const AttnArgs a) {
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int H = a.num_heads;
-  if (w >= (int64_t)a.n_q * H) return;
-  const int64_t row = w / H;
-  const int h = (int)(w - row * H);
+  constexpr int TPR = D / 4;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t rh = gid / TPR;                      // row * H + head
+  const int c = (int)(gid - rh * TPR);
+  const int64_t n_rh = (int64_t)a.n_q * a.num_heads;
+  if (rh >= n_rh) return;
+  const float* lse = a.part_lse + rh;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + rh * D) + c;
+  const int64_t po_stride = n_rh * (D / 4);
   float mx = -INFINITY;
-  for (int s = 0; s < a.n_splits; ++s) mx = fmaxf(mx, a.part_lse[((int64_t)s * a.n_q + row) * H + h]);
+#pragma unroll 8
+  for (int s = 0; s < a.n_splits; ++s) mx = fmaxf(mx, __ldg(lse + s * n_rh));
   float wsum = 0.f;
-  float o[D / 32];
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) o[i] = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
   for (int s = 0; s < a.n_splits; ++s) {
-    const float wt = exp2f(a.part_lse[((int64_t)s * a.n_q + row) * H + h] - mx);
+    const float wt = exp2f(__ldg(lse + s * n_rh) - mx);
+    const float4 p = __ldg(po + s * po_stride);
     wsum += wt;
-    const float* po = a.part_o + (((int64_t)s * a.n_q + row) * H + h) * D;
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) o[i] = fmaf(wt, po[lane + 32 * i], o[i]);
+    o.x = fmaf(wt, p.x, o.x);
+    o.y = fmaf(wt, p.y, o.y);
+    o.z = fmaf(wt, p.z, o.z);
+    o.w = fmaf(wt, p.w, o.w);
   }
   const float inv = 1.f / wsum;
-  T* op = reinterpret_cast<T*>(a.out) + (row * H + h) * D;
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) op[lane + 32 * i] = from_f<T>(o[i] * inv);
+  T* op = reinterpret_cast<T*>(a.out) + rh * D + 4 * c;
+  op[0] = from_f<T>(o.x * inv);
+  op[1] = from_f<T>(o.y * inv);
+  op[2] = from_f<T>(o.z * inv);
+  op[3] = from_f<T>(o.w * inv);
 }
 
 template <typename T, int D>
@@ -240,9 +251,11 @@ cudaError_t simt_by_dim(const AttnArgs& a, cudaStream_t st) {
 
 template <typename T>
 cudaError_t merge_by_dim(const AttnArgs& a, cudaStream_t st) {
-  const int64_t warps = (int64_t)a.n_q * a.num_heads;
+  const int64_t n_rh = (int64_t)a.n_q * a.num_heads;
   const int threads = 256;
-  const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
+  // D / 4 threads per (row, head)
+  const unsigned blocks = (unsigned)((n_rh * (a.head_dim / 4) + threads - 1) / threads);
+  if (blocks == 0) return cudaSuccess;
   switch (a.head_dim) {
     case 32: merge_kernel<T, 32><<<blocks, threads, 0, st>>>(a); break;
     case 64: merge_kernel<T, 64><<<blocks, threads, 0, st>>>(a); break;
