@@ -42,7 +42,8 @@ def parse():
     p.add_argument("--steps", type=int, default=None, help="timed frames (default: rest of the stream)")
     p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="s518")
+    p.add_argument("--workload", default="s518",
+                   help="s518 (default, the streamed metric), another streaming workload, or phase1")
     p.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     p.add_argument("--pool", type=int, default=4, help="distinct input frames per layer")
     p.add_argument("--seed", type=int, default=0)
@@ -320,6 +321,100 @@ def run_ours(args, rank, world):
     return res
 
 
+PHASE1_METRIC = ("Phase-1 batch prefill frames/s (8 scale frames x 1005 tokens, dense bidirectional, "
+                 "24-layer paged attn, 518x378); attn TFLOP/s vs GB300 roofline")
+
+
+def run_phase1(args, rank, world):
+    """Phase 1 (batch mode): every layer's first 8 frames attend to each other
+    densely (8 x 1005 = 8040 queries over the same 8040 keys) and are appended
+    (kvc_prefill).  One step = kvc_clean + the prefill of every layer."""
+    import torch
+    from streaming_paged_kv_gb300 import build
+    build.build()
+    from streaming_paged_kv_gb300 import kvc
+    from streaming_paged_kv_gb300.inputs import frame_qkv, k_head_scale
+    from streaming_paged_kv_gb300.workloads import WORKLOADS
+    w = WORKLOADS["s518"]
+    L = args.layers or w.num_layers
+    F, T, H, D = w.scale_frames, w.tokens_per_frame, w.num_heads, w.head_dim
+    n_q = F * T
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    K = args.steps if args.steps is not None else 20
+    W = max(args.warmup, 3)
+    c = kvc.PagedKVCache(L, H, D, w.page_size, w.dtype, w.scale_frames, w.sliding_window, w.headroom,
+                         w.max_total_frames, max_query_tokens=n_q)
+    if args.kernel:
+        c.set_option(kvc.KVC_OPT_ATTN_KERNEL, args.kernel)
+    hs = k_head_scale(args.seed + rank, w.wid, H)
+    inputs = []
+    for layer in range(min(args.pool, L)):
+        fr = [frame_qkv(args.seed + rank, w.wid, f, layer, w.page_size, H, D, w.dtype, hs) for f in range(F)]
+        inputs.append(tuple(torch.cat([x[i] for x in fr]).to(dev) for i in range(3)))
+    out = torch.empty_like(inputs[0][0])
+
+    def step():
+        c.clean()
+        for layer in range(L):
+            q, k, v = inputs[layer % len(inputs)]
+            c.prefill(layer, q, k, v, out)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    kvc.kvc_get_counters(c.h, reset=True)
+    c.set_option(kvc.KVC_OPT_TIMING, 1)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(K):
+        step()
+    ev1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms, total_steps = aggregate(ev0.elapsed_time(ev1), K, world, dev)
+    launches, attn_launches, attn_ms = kvc.kvc_get_counters(c.h, reset=True)
+    c.set_option(kvc.KVC_OPT_TIMING, 0)
+    if kvc.kvc_device_status(c.h, c._stream()) != 0:
+        raise RuntimeError("device status")
+    flops = K * L * 4.0 * n_q * n_q * H * D
+    bytes_alg = K * L * (2.0 * n_q * H * D * 2 + 2.0 * n_q * H * D * 2)
+    pk = peaks()
+    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
+    c.close()
+    return {
+        "metric": PHASE1_METRIC, "value": total_steps * F / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"phase1_518: {F} scale frames x {T} tokens, {L} layers, H={H}, D={D}, "
+                               f"page_size={w.page_size}; one step = clean + prefill of every layer",
+                   "l2": "no flush: the layers' caches (33 MB of K/V each, 24 blocks) exceed L2 together",
+                   "parallelism": f"replicas x{world} (independent streams, no collective)"},
+        "roofline": {
+            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None, "traffic": None,
+            "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
+            "kernel": "paged attention (kvc_run attention launch inside kvc_prefill)",
+            "flops_per_launch": flops / max(attn_launches, 1),
+            "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
+            "launch_ms": attn_ms / max(attn_launches, 1)},
+        "attn_tflops": achieved,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+
+
 def run_e2e(args, kvc, w, dev, rank, world):
     """The same frames/s through the public API with host inputs: every step
     copies that frame's Q/K/V of every layer from pinned host memory and reads
@@ -497,6 +592,15 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
+    if args.workload == "phase1":
+        res = run_phase1(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return 0
     res = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:

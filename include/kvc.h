@@ -168,6 +168,23 @@ int kvc_plan(kvc_handle* h, kvc_stream stream);
  * pages differ from the plan's), INVALID_ARG, CUDA. */
 int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q, kvc_stream stream);
 
+/* Phase 1, batch mode ([KVC] "FlashInferAttention Layer Implementation";
+ * [SLOTS] "scale frames永不驱逐"): the first n_frames frames attend to each
+ * other densely and bidirectionally as one block, then are appended frame by
+ * frame.  K and V are [n_frames * (6 + page_size), H, D], frame after frame,
+ * each frame laid out as kvc_append_frame expects; Q and out are the same
+ * shape.  The block must be empty (fresh, or after kvc_clean).  The frames
+ * are appended (no eviction), then -- for block 0 -- the plan is rebuilt, and
+ * the queries attend over the block's visible tokens, which are exactly the
+ * n_frames frames' tokens; the result is the dense attention because the
+ * order of keys does not change a softmax-weighted sum.  Blocks other than 0
+ * use block 0's plan, as in streaming, so block 0 is prefilled first.
+ * n_frames * (6 + page_size) <= max_query_tokens.  Errors: INVALID_ARG (block
+ * not empty, sizes, pointers), NO_FREE_PAGE, SPECIAL_POOL_FULL, STALE_PLAN,
+ * NO_DEVICE, CUDA; on an error the block's bookkeeping is left unchanged. */
+int kvc_prefill(kvc_handle* h, int32_t block, const void* Q, const void* K, const void* V, int32_t n_frames,
+                void* out, kvc_stream stream);
+
 /* get_cache_stats(block_idx) ([SLOTS] "动手验证"). */
 int kvc_get_cache_stats(const kvc_handle* h, int32_t block, kvc_stats* out);
 

@@ -14,7 +14,9 @@ What it computes, in plain slow code:
   and a byte-exact NumPy mirror of the cache tensor
   ``[max_num_pages, 2, page_size, H, D]``.
 * ``oracle.attention`` -- softmax attention of a frame's queries over the
-  visible keys/values, gathered densely in page order and computed in float64.
+  visible keys/values, gathered densely in page order and computed in float64;
+  and Phase 1 (batch mode): dense bidirectional attention of the first frames
+  as one block, from the frames' own Q/K/V.
 
 Pages cited (by tag, then section):
 
@@ -43,4 +45,4 @@ Readings taken where the pages are silent (each also listed in the design doc):
 """
 
 from .paged_kv import OraclePagedKV, OracleError  # noqa: F401
-from .attention import dense_attention, paged_attention  # noqa: F401
+from .attention import dense_attention, paged_attention, prefill_attention  # noqa: F401

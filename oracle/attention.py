@@ -69,3 +69,20 @@ def paged_attention(cache, block, q_bits, sm_scale=None, rows=None, plan_block=0
         q = q[np.asarray(rows)]
     return dense_attention(q, bits_to_f64(k_bits, cache.dtype),
                            bits_to_f64(v_bits, cache.dtype), sm_scale)
+
+
+def prefill_attention(q_frames, k_frames, v_frames, dtype, sm_scale=None, rows=None):
+    """Phase 1, batch mode ([KVC] "FlashInferAttention Layer Implementation";
+    [SLOTS] "scale frames永不驱逐"): the first frames go through standard dense
+    attention as one block, bidirectionally -- every query of every frame over
+    every key of every frame.  Inputs are the frames' raw bits, each
+    ``[T, H, D]``; the result is ``[F*T, H, D]`` float64, frame after frame
+    (only the query rows ``rows`` of that, if given).
+    """
+    q = np.concatenate([bits_to_f64(x, dtype) for x in q_frames])
+    if rows is not None:
+        q = q[np.asarray(rows)]
+    k = np.concatenate([bits_to_f64(x, dtype) for x in k_frames])
+    v = np.concatenate([bits_to_f64(x, dtype) for x in v_frames])
+    return dense_attention(q, k, v, sm_scale)
+

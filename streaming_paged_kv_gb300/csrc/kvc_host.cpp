@@ -523,6 +523,45 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
   return KVC_OK;
 }
 
+// Phase 1 ([KVC] "FlashInferAttention Layer Implementation", batch mode;
+// [SLOTS] "scale frames永不驱逐"): dense bidirectional attention of the first
+// frames as one block, then append_frame per frame.  Appending the frames to
+// an empty block first makes its visible set exactly their n_frames * T
+// tokens, and non-causal attention over a set does not depend on the order
+// of its keys, so the paged kernel computes the dense attention.
+int kvc_prefill(kvc_handle* h, int32_t block, const void* Q, const void* K, const void* V, int32_t n_frames,
+                void* out, kvc_stream stream) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  if (!h->device) return KVC_ERR_NO_DEVICE;
+  const Block& b = h->blocks[block];
+  if (n_frames < 1 || b.frame_count != 0 || b.special_frames != 0 || b.scale.size != 0 || b.live.size != 0)
+    return KVC_ERR_INVALID_ARG;
+  const int64_t n_q = (int64_t)n_frames * h->g.T;
+  if (n_q > h->cfg.max_query_tokens) return KVC_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !out || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
+    return KVC_ERR_INVALID_ARG;
+  if (n_frames > b.free_list.size) return KVC_ERR_NO_FREE_PAGE;
+  if (n_frames > h->cfg.max_total_frames) return KVC_ERR_SPECIAL_POOL_FULL;
+  const int64_t frame_bytes = h->g.T * h->g.row_bytes;
+  int32_t appended = 0;
+  for (; appended < n_frames; ++appended) {
+    rc = kvc_append_frame(h, block, (const char*)K + appended * frame_bytes,
+                          (const char*)V + appended * frame_bytes, stream);
+    if (rc) break;
+  }
+  bool planned = false;
+  if (rc == KVC_OK && block == 0) planned = (rc = kvc_plan(h, stream)) == KVC_OK;
+  if (rc == KVC_OK) rc = kvc_run(h, block, Q, out, (int32_t)n_q, stream);
+  if (rc != KVC_OK) {
+    // Leave the bookkeeping as it was (cache bytes are not part of it); a
+    // plan made here described the frames just undone, so it is dropped.
+    for (int32_t f = 0; f < appended; ++f) kvc_rollback_last_frame(h, block);
+    if (planned) h->has_plan = false;
+  }
+  return rc;
+}
+
 int kvc_get_cache_stats(const kvc_handle* h, int32_t block, kvc_stats* out) {
   int rc = check_block(h, block);
   if (rc) return rc;

@@ -72,6 +72,7 @@ _SIGS = {
     "kvc_clean": [_P],
     "kvc_plan": [_P, _P],
     "kvc_run": [_P, _I32, _P, _P, _I32, _P],
+    "kvc_prefill": [_P, _I32, _P, _P, _P, _I32, _P, _P],
     "kvc_get_cache_stats": [_P, _I32, ctypes.POINTER(kvc_stats)],
     "kvc_get_plan": [_P, _PI32, _PI32, _I32, _PI32, _PI32],
     "kvc_get_deques": [_P, _I32, _PI32, _PI32, _PI32, _PI32, _PI32, _PI32],
@@ -156,6 +157,10 @@ def kvc_plan(h, stream=None):
 
 def kvc_run(h, block, q_ptr, out_ptr, n_q, stream=None):
     return _check(lib.kvc_run(h, block, q_ptr, out_ptr, n_q, stream), "kvc_run")
+
+
+def kvc_prefill(h, block, q_ptr, k_ptr, v_ptr, n_frames, out_ptr, stream=None):
+    return _check(lib.kvc_prefill(h, block, q_ptr, k_ptr, v_ptr, n_frames, out_ptr, stream), "kvc_prefill")
 
 
 def kvc_get_cache_stats(h, block):
@@ -305,6 +310,16 @@ class PagedKVCache:
 
     def run(self, block, q, out):
         kvc_run(self.h, block, self._ptr(q), self._ptr(out), q.shape[0], self._stream())
+        return out
+
+    def prefill(self, block, q, k, v, out):
+        """Phase 1: n_frames = q.shape[0] // (6 + page_size) frames attend to each
+        other densely, then are appended to the (empty) block."""
+        T = 6 + self.page_size
+        if q.shape[0] % T or k.shape != q.shape or v.shape != q.shape or out.shape != q.shape:
+            raise ValueError("prefill wants Q, K, V, out of shape [n_frames * (6 + page_size), H, D]")
+        kvc_prefill(self.h, block, self._ptr(q), self._ptr(k), self._ptr(v), q.shape[0] // T,
+                    self._ptr(out), self._stream())
         return out
 
     def stats(self, block):

@@ -19,7 +19,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import OraclePagedKV, OracleError, dense_attention, paged_attention
+from oracle import OraclePagedKV, OracleError, dense_attention, paged_attention, prefill_attention
 from oracle.attention import bits_to_f64
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_facts.json")
@@ -389,6 +389,38 @@ def _check_attention(fn):
 def test_dense_attention_pins():
     r = _check_attention(dense_attention)
     assert max(r.values()) < 1e-12, r
+
+
+def test_prefill_is_paged_attention_of_an_empty_cache_after_the_appends():
+    """Phase 1 ([KVC] "FlashInferAttention Layer Implementation"): dense
+    attention over the frames' own tokens.  Appending them to an empty cache
+    makes the visible set exactly those tokens (in page order: patches of each
+    frame, then the specials), so the oracle's paged path -- gathered pages,
+    written independently of the concatenation -- must give the same result;
+    so must any reordering of the frames' keys.  Bidirectional: frame 0's
+    queries depend on the last frame's values."""
+    from streaming_paged_kv_gb300.inputs import frame_qkv, to_bits
+    F, ps, H, D = 3, 16, 2, 32
+    frames = [frame_qkv(7, 1, f, 0, ps, H, D, "f32") for f in range(F)]
+    qb = [to_bits(q) for q, _, _ in frames]
+    kb = [to_bits(k) for _, k, _ in frames]
+    vb = [to_bits(v) for _, _, v in frames]
+    want = prefill_attention(qb, kb, vb, "f32")
+    orc = OraclePagedKV(1, ps, H, D, "f32", 2, 4, 2, 16)
+    for f in range(F):
+        orc.append_frame(0, kb[f], vb[f])
+    paged = paged_attention(orc, 0, np.concatenate(qb))
+    assert np.abs(paged - want).max() < 1e-12
+    perm = [2, 0, 1]
+    shuffled = dense_attention(bits_to_f64(np.concatenate(qb), "f32"),
+                               bits_to_f64(np.concatenate([kb[i] for i in perm]), "f32"),
+                               bits_to_f64(np.concatenate([vb[i] for i in perm]), "f32"))
+    assert np.abs(shuffled - want).max() < 1e-12
+    vb2 = list(vb)
+    vb2[F - 1] = to_bits(frames[F - 1][2] + 1.0)
+    changed = prefill_attention(qb, kb, vb2, "f32")
+    T = ps + 6
+    assert np.abs(changed[:T] - want[:T]).max() > 1e-3   # frame 0 sees the last frame
 
 
 def test_bf16_and_f16_decoding_matches_torch():
