@@ -43,9 +43,10 @@ def parse():
     p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="s518",
-                   help="s518 (default, the streamed metric), another streaming workload, or phase1")
+                   help="s518 (default, the streamed metric), another streaming workload, phase1 or batch224")
     p.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     p.add_argument("--pool", type=int, default=4, help="distinct input frames per layer")
+    p.add_argument("--batch", type=int, default=8, help="streams of --workload batch224")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=64)
     p.add_argument("--no-e2e", action="store_true")
@@ -415,6 +416,112 @@ def run_phase1(args, rank, world):
     }
 
 
+BATCH_METRIC = ("batched streams frames/s (B independent 224x224 streams, one attention launch per layer, "
+                "24-layer paged attn); attn TFLOP/s vs GB300 roofline")
+
+
+def run_batch224(args, rank, world):
+    """Several independent 224x224 streams (one handle each) advance in
+    lockstep; per layer every stream appends, evicts and (block 0) plans, then
+    one kvc_run_batch launch attends all of them.  Timed region: frames
+    (steady state, full window) of every stream."""
+    import torch
+    from streaming_paged_kv_gb300 import build
+    build.build()
+    from streaming_paged_kv_gb300 import kvc
+    from streaming_paged_kv_gb300.workloads import WORKLOADS
+    w = WORKLOADS["s224"]
+    if args.layers:
+        w = w.with_(num_layers=args.layers)
+    B = args.batch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    K = args.steps if args.steps is not None else 60
+    W = max(args.warmup, 3)
+    start = w.n_frames - K - W        # the timed frames are the stream's last K
+    streams = [Stream(kvc, w, args.pool, args.seed + rank * 64 + i, args.kernel, dev) for i in range(B)]
+    for st in streams:
+        st.fast_forward(start)
+    T, H, D, L = w.tokens_per_frame, w.num_heads, w.head_dim, w.num_layers
+    rows = [T] * B
+    qcat = [[torch.cat([st.inputs(f, b)[0] for st in streams]) for b in range(L)] for f in range(args.pool)]
+    out = torch.empty(B * T, H, D, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        f = streams[0].frame
+        for b in range(L):
+            for st in streams:
+                _, k, v = st.inputs(st.frame, b)
+                st.c.append_frame(b, k, v)
+                st.c.evict_frames(b)
+                if b == 0:
+                    st.c.plan()
+            kvc.run_batch([st.c for st in streams], [b] * B, qcat[(f + b) % args.pool][b], out, rows)
+        for st in streams:
+            st.frame += 1
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    nkv = streams[0].visible_tokens()     # every stream is in the same steady state
+    flops = K * L * B * 4.0 * T * nkv * H * D
+    bytes_alg = K * L * B * (2.0 * nkv * H * D * 2 + 2.0 * T * H * D * 2)
+    h0 = streams[0].c
+    kvc.kvc_get_counters(h0.h, reset=True)
+    h0.set_option(kvc.KVC_OPT_TIMING, 1)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(K):
+        step()
+    ev1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms, total_steps = aggregate(ev0.elapsed_time(ev1), K, world, dev)
+    _, attn_launches, attn_ms = kvc.kvc_get_counters(h0.h, reset=True)
+    launches = sum(kvc.kvc_get_counters(st.c.h, reset=True)[0] for st in streams) + _
+    h0.set_option(kvc.KVC_OPT_TIMING, 0)
+    for st in streams:
+        if kvc.kvc_device_status(st.c.h, st.c._stream()) != 0:
+            raise RuntimeError("device status")
+    pk = peaks()
+    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
+    res = {
+        "metric": BATCH_METRIC, "value": total_steps * B / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"batch224: {B} streams x 224x224 (H={H}, D={D}, page_size={w.page_size}), "
+                               f"{L} layers, frames {start + W}..{start + W + K - 1} of each {w.n_frames}-frame "
+                               f"stream ({nkv} visible tokens)",
+                   "l2": "no flush: the streams' visible K/V per layer together exceed L2",
+                   "parallelism": f"replicas x{world} (independent streams, no collective)"},
+        "roofline": {
+            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None, "traffic": None,
+            "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
+            "kernel": "paged attention (one kvc_run_batch launch per layer)",
+            "flops_per_launch": flops / max(attn_launches, 1),
+            "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
+            "launch_ms": attn_ms / max(attn_launches, 1)},
+        "attn_tflops": achieved,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    del streams
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_e2e(args, kvc, w, dev, rank, world):
     """The same frames/s through the public API with host inputs: every step
     copies that frame's Q/K/V of every layer from pinned host memory and reads
@@ -592,8 +699,8 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    if args.workload == "phase1":
-        res = run_phase1(args, rank, world)
+    if args.workload in ("phase1", "batch224"):
+        res = (run_phase1 if args.workload == "phase1" else run_batch224)(args, rank, world)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if world > 1:

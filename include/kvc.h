@@ -168,6 +168,24 @@ int kvc_plan(kvc_handle* h, kvc_stream stream);
  * pages differ from the plan's), INVALID_ARG, CUDA. */
 int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q, kvc_stream stream);
 
+/* Several independent streams in one launch.  FlashInfer's batch plan takes
+ * a qo_indptr with one entry per request ([KVC] "Kernel-Level Execution
+ * Flow"); the pages only ever pass one, so this call has no counterpart there
+ * beyond that signature.  Request r (0 <= r < count <= 16) is handle hs[r]'s
+ * block blocks[r] with query rows [qo_indptr[r], qo_indptr[r+1]) of Q and out
+ * ([qo_indptr[count], H, D], the dtype of every handle).  The handles are
+ * distinct, share num_heads, head_dim, dtype and sm_scale, and each has a
+ * current plan for its block (as kvc_run requires).  With the tensor-core
+ * kernel all requests go into one launch, with one KV split count chosen for
+ * the whole batch (each handle's partial buffers hold its own request's
+ * splits); otherwise the requests run one after another.  Launch counters and
+ * KVC_OPT_TIMING are kept by hs[0].  qo_indptr is a host array.  Errors:
+ * INVALID_ARG (count, pointers, qo_indptr not starting at 0 or decreasing,
+ * repeated handles, different geometry), and for the first failing request
+ * those of kvc_run -- nothing is launched then. */
+int kvc_run_batch(kvc_handle* const* hs, const int32_t* blocks, int32_t count, const void* Q, void* out,
+                  const int32_t* qo_indptr, kvc_stream stream);
+
 /* Phase 1, batch mode ([KVC] "FlashInferAttention Layer Implementation";
  * [SLOTS] "scale frames永不驱逐"): the first n_frames frames attend to each
  * other densely and bidirectionally as one block, then are appended frame by

@@ -50,6 +50,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdlib>
+#include <cstring>
 #include <new>
 #include <type_traits>
 
@@ -358,10 +359,32 @@ __device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&v)[N]) {
   tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[OFF]));
 }
 
+// One launch serves up to kTcMaxBatch independent requests (streams, each with
+// its own cache, plan and split-KV partials).  Everything a CTA needs is in the
+// launch parameters; the grid is one-dimensional and request r owns CTAs
+// [cta0, cta0 + q_blocks * H * n_splits), ordered query block fastest, then
+// head, then split.
+struct TcRequest {
+  const KvTile* tiles;
+  float* part_o;           // [n_splits][n_q][H][D] (n_splits > 1)
+  float* part_lse;         // [n_splits][n_q][H]
+  int32_t* status;
+  int32_t n_tiles, n_splits, q_row0, n_q, page_base, cta0, q_blocks, pad;
+};
+struct TcLaunch {
+  CUtensorMap q_map;       // [rows, H * D] over every request's query rows
+  CUtensorMap cache_map[kTcMaxBatch];   // 3D view of each request's whole cache
+  void* out;               // [rows, H, D]
+  int32_t count, num_heads, stall_test, pad;
+  float sm_scale_log2;
+  long long wait_budget;
+  TcRequest req[kTcMaxBatch];
+};
+static_assert(sizeof(TcLaunch) <= 4000, "kernel parameter space");
+
 template <bool BF16>
 __global__ void __launch_bounds__(REG_BOUND_THREADS, 1)
-attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
-               const __grid_constant__ CUtensorMap q_map, int32_t page_base) {
+attn_tc_kernel(const __grid_constant__ TcLaunch P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + OFF_Q;
@@ -388,15 +411,24 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y, split = blockIdx.z;
-  const int q0 = blockIdx.x * (QT * BM);
-  const bool has_q1 = q0 + BM < a.n_q;
+  // Which request, query block, head and split this CTA serves.
+  int rq = 0;
+  while (rq + 1 < P.count && (int)blockIdx.x >= P.req[rq + 1].cta0) ++rq;
+  const TcRequest& R = P.req[rq];
+  const int local = (int)blockIdx.x - R.cta0;
+  const int qblock = local % R.q_blocks;
+  const int h = (local / R.q_blocks) % P.num_heads;
+  const int split = local / (R.q_blocks * P.num_heads);
+  const int q0 = qblock * (QT * BM);              // first query row within the request
+  const bool has_q1 = q0 + BM < R.n_q;
   const int nq = has_q1 ? 2 : 1;
-  const int t0 = (int)(((int64_t)split * a.n_tiles) / a.n_splits);
-  const int t1 = (int)(((int64_t)(split + 1) * a.n_tiles) / a.n_splits);
+  const int t0 = (int)(((int64_t)split * R.n_tiles) / R.n_splits);
+  const int t1 = (int)(((int64_t)(split + 1) * R.n_tiles) / R.n_splits);
   const int n = t1 - t0;
   const int n_s = n * nq;                         // score tiles of this CTA
-  Guard g{abort_flag, a.status, a.wait_budget};
+  const KvTile* tiles = R.tiles;
+  const CUtensorMap* cache_map = &P.cache_map[rq];
+  Guard g{abort_flag, R.status, P.wait_budget};
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -436,18 +468,18 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
       int issued = 0;
       if (leader) {
         mbar_expect_tx(q_full, nq * Q_BYTES);
-        tma_load_2d(sQ, &q_map, h * HD, q0, q_full);
-        if (has_q1) tma_load_2d(sQ + Q_BYTES, &q_map, h * HD, q0 + BM, q_full);
+        tma_load_2d(sQ, &P.q_map, h * HD, R.q_row0 + q0, q_full);
+        if (has_q1) tma_load_2d(sQ + Q_BYTES, &P.q_map, h * HD, R.q_row0 + q0 + BM, q_full);
       }
       for (int j = 0; j < n; ++j) {
         const int st = j % STAGES;
         if (j >= STAGES && !wait_bar_warp(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
-        const KvTile tile = a.tiles[t0 + j];
-        const int plane = (page_base + tile.page) * 2;
+        const KvTile tile = tiles[t0 + j];
+        const int plane = (R.page_base + tile.page) * 2;
         if (leader) {
           mbar_expect_tx(&kv_full[st], 2 * TILE_BYTES);
-          tma_load_3d(sK + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane, &kv_full[st]);
-          tma_load_3d(sV + st * TILE_BYTES, &cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
+          tma_load_3d(sK + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane, &kv_full[st]);
+          tma_load_3d(sV + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
         }
         issued = j + 1;
       }
@@ -519,7 +551,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
         constexpr uint32_t IDESC_O = idesc_f16(BM, HD, BF16, true);
         const uint64_t dV0 = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
         uint32_t p_par = 0;
-        ok = !a.stall_test || wait_bar_warp(g, never, 0, 12);
+        ok = !P.stall_test || wait_bar_warp(g, never, 0, 12);
         for (int k = 0, j = 0; ok && k < n_s; ++k) {
           if (i == 0) {
             // V(j) landed (already true in practice: S(k) needed K(j) of the same copy).
@@ -566,17 +598,17 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
     const int r = quarter * 32 + lane;               // query row within the tile == TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t O_ = lane_base + o_col(qi);
-    const float sl2 = a.sm_scale_log2;
+    const float sl2 = P.sm_scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     float m_ref = -INFINITY;
     uint64_t la = 0, lb = 0;                         // row-sum partials (two fp32 pairs)
     bool ok = n > 0 && qi < nq;                      // warp-uniform
 
-    int rows_next = ok ? a.tiles[t0].rows : 0;
+    int rows_next = ok ? tiles[t0].rows : 0;
     for (int j = 0; ok && j < n; ++j) {
       const int k = j * nq + qi, b = k % NBUF;
       const int rows_valid = rows_next;
-      if (j + 1 < n) rows_next = a.tiles[t0 + j + 1].rows;   // prefetch for the next tile
+      if (j + 1 < n) rows_next = tiles[t0 + j + 1].rows;   // prefetch for the next tile
       ok = wait_bar_warp(g, &s_full[b], (k / NBUF) & 1, 6);
       if (!ok) break;
       tc_fence_after();
@@ -664,12 +696,13 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < HD; ++c) asm volatile("" : "+r"(v[c])::"memory");
-        const int row = q0 + qi * BM + r;
-        if (row < a.n_q) {
+        const int row = q0 + qi * BM + r;             // within the request
+        if (row < R.n_q) {
           const float inv = 1.f / l;
-          if (a.n_splits == 1) {
+          if (R.n_splits == 1) {
             using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.out) + ((int64_t)row * a.num_heads + h) * HD);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(P.out) +
+                                                  ((int64_t)(R.q_row0 + row) * P.num_heads + h) * HD);
 #pragma unroll
             for (int i = 0; i < HD / 8; ++i) {
               const float* o = reinterpret_cast<const float*>(&v[8 * i]);
@@ -681,12 +714,12 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap cache_map,
               dst[i] = u;
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(a.part_o + (((int64_t)split * a.n_q + row) * a.num_heads + h) * HD);
+            float4* dst = reinterpret_cast<float4*>(R.part_o + (((int64_t)split * R.n_q + row) * P.num_heads + h) * HD);
 #pragma unroll
             for (int i = 0; i < HD / 4; ++i)
               dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
                                    __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
-            a.part_lse[((int64_t)split * a.n_q + row) * a.num_heads + h] = m_ref + __log2f(l);
+            R.part_lse[((int64_t)split * R.n_q + row) * P.num_heads + h] = m_ref + __log2f(l);
           }
         }
       }
@@ -766,37 +799,56 @@ TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, in
 
 void tc_destroy_maps(TcMaps* m) { delete m; }
 
-cudaError_t launch_attn_tc(const AttnArgs& a, TcMaps* maps, int block, int max_pages, int dtype,
-                           cudaStream_t stream) {
+cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
-  if (!enc || !maps || a.head_dim != HD) return cudaErrorNotSupported;
-  CUtensorMap qmap;
-  const cuuint64_t row_bytes = (cuuint64_t)a.num_heads * HD * 2;
-  cuuint64_t dims[2] = {(cuuint64_t)a.num_heads * HD, (cuuint64_t)a.n_q};
+  if (!enc || b.count < 1 || b.count > kTcMaxBatch || b.head_dim != HD) return cudaErrorNotSupported;
+  TcLaunch P;
+  std::memset(&P, 0, sizeof(P));
+  const cuuint64_t row_bytes = (cuuint64_t)b.num_heads * HD * 2;
+  cuuint64_t dims[2] = {(cuuint64_t)b.num_heads * HD, (cuuint64_t)b.rows};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {HD, BM};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&qmap, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                   const_cast<void*>(a.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  dim3 grid((a.n_q + QT * BM - 1) / (QT * BM), a.num_heads, a.n_splits);
-  const int page_base = block * max_pages;
-  if (dtype == 0) {
-    if (!configured_smem[0]) {
-      cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-      configured_smem[0] = true;
-    }
-    attn_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, maps->cache, qmap, page_base);
-  } else {
-    if (!configured_smem[1]) {
-      cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-      configured_smem[1] = true;
-    }
-    attn_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(a, maps->cache, qmap, page_base);
+  CUresult cr = enc(&P.q_map, b.dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(b.q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  P.out = b.out;
+  P.count = b.count;
+  P.num_heads = b.num_heads;
+  P.stall_test = b.stall_test;
+  P.sm_scale_log2 = b.sm_scale_log2;
+  P.wait_budget = b.wait_budget;
+  int64_t ctas = 0;
+  for (int r = 0; r < b.count; ++r) {
+    const TcRequestDesc& d = b.req[r];
+    if (!d.maps || d.n_q < 0 || d.n_splits < 1 || d.q_row0 < 0 || d.q_row0 + d.n_q > b.rows)
+      return cudaErrorInvalidValue;
+    TcRequest& q = P.req[r];
+    P.cache_map[r] = d.maps->cache;
+    q.tiles = d.tiles;
+    q.part_o = d.part_o;
+    q.part_lse = d.part_lse;
+    q.status = d.status;
+    q.n_tiles = d.n_tiles;
+    q.n_splits = d.n_splits;
+    q.q_row0 = d.q_row0;
+    q.n_q = d.n_q;
+    q.page_base = d.block * d.max_pages;
+    q.q_blocks = (d.n_q + QT * BM - 1) / (QT * BM);
+    q.cta0 = (int32_t)ctas;
+    ctas += (int64_t)q.q_blocks * b.num_heads * d.n_splits;
   }
+  if (ctas == 0) return cudaSuccess;
+  if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+  const int which = b.dtype == 0 ? 0 : 1;
+  auto kernel = which == 0 ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  if (!configured_smem[which]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured_smem[which] = true;
+  }
+  kernel<<<(unsigned)ctas, NUM_THREADS, SMEM_BYTES, stream>>>(P);
   return cudaGetLastError();
 }
 

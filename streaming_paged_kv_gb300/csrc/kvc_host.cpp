@@ -251,6 +251,79 @@ void drain_timing(kvc_handle* h) {
 
 }  // namespace
 
+// Preconditions of a run: a device handle, a plan, this block's pages equal
+// to the planned ones, n_q within limits, aligned buffers.
+int check_run(const kvc_handle* h, int32_t block, const void* Q, const void* out, int32_t n_q) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  if (!h->device) return KVC_ERR_NO_DEVICE;
+  if (!h->has_plan) return KVC_ERR_NO_PLAN;
+  if (n_q < 0 || n_q > h->cfg.max_query_tokens) return KVC_ERR_INVALID_ARG;
+  if (n_q > 0 && (!Q || !out || !aligned16(Q) || !aligned16(out))) return KVC_ERR_INVALID_ARG;
+  // The plan is valid for this block only if its pages are the planned ones.
+  const Block& b = h->blocks[block];
+  if (b.scale.size != h->plan_n_scale || b.live.size != h->plan_n_live ||
+      b.special_frames != h->plan_special_frames)
+    return KVC_ERR_STALE_PLAN;
+  for (int32_t i = 0; i < b.scale.size; ++i)
+    if (b.scale.at(i) != h->plan_snapshot[i]) return KVC_ERR_STALE_PLAN;
+  for (int32_t i = 0; i < b.live.size; ++i)
+    if (b.live.at(i) != h->plan_snapshot[b.scale.size + i]) return KVC_ERR_STALE_PLAN;
+  return KVC_OK;
+}
+
+kvc::AttnArgs attn_args(const kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q, int splits) {
+  kvc::AttnArgs a;
+  a.q = Q;
+  a.out = out;
+  a.cache = h->cache + (size_t)block * h->g.block_bytes;
+  a.tiles = (const kvc::KvTile*)(h->ws + h->g.L.tiles);
+  a.part_o = (float*)(h->ws + h->g.L.part_o);
+  a.part_lse = (float*)(h->ws + h->g.L.part_lse);
+  a.status = (int32_t*)(h->ws + h->g.L.status);
+  a.n_q = n_q;
+  a.num_heads = h->cfg.num_heads;
+  a.head_dim = h->cfg.head_dim;
+  a.page_size = h->cfg.page_size;
+  a.n_tiles = h->plan_n_tiles;
+  a.n_splits = splits;
+  a.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
+  a.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
+  a.stall_test = h->stall_test;
+  return a;
+}
+
+kvc::TcBatchArgs tc_batch_header(const kvc_handle* h, const void* Q, void* out, int32_t rows) {
+  kvc::TcBatchArgs tb;
+  std::memset(&tb, 0, sizeof(tb));
+  tb.q = Q;
+  tb.out = out;
+  tb.rows = rows;
+  tb.num_heads = h->cfg.num_heads;
+  tb.head_dim = h->cfg.head_dim;
+  tb.dtype = h->cfg.dtype;
+  tb.stall_test = h->stall_test;
+  tb.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
+  tb.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
+  return tb;
+}
+
+kvc::TcRequestDesc tc_request(const kvc_handle* h, int32_t block, int32_t q_row0, int32_t n_q, int splits) {
+  kvc::TcRequestDesc d;
+  d.maps = h->maps;
+  d.block = block;
+  d.max_pages = h->g.max_pages;
+  d.tiles = (const kvc::KvTile*)(h->ws + h->g.L.tiles);
+  d.part_o = (float*)(h->ws + h->g.L.part_o);
+  d.part_lse = (float*)(h->ws + h->g.L.part_lse);
+  d.status = (int32_t*)(h->ws + h->g.L.status);
+  d.n_tiles = h->plan_n_tiles;
+  d.n_splits = splits;
+  d.q_row0 = q_row0;
+  d.n_q = n_q;
+  return d;
+}
+
 extern "C" {
 
 int kvc_required_bytes(const kvc_config* cfg, size_t* cache_bytes, size_t* workspace_bytes) {
@@ -472,45 +545,22 @@ int kvc_plan(kvc_handle* h, kvc_stream stream) {
 }
 
 int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q, kvc_stream stream) {
-  int rc = check_block(h, block);
-  if (rc) return rc;
-  if (!h->device) return KVC_ERR_NO_DEVICE;
-  if (!h->has_plan) return KVC_ERR_NO_PLAN;
-  if (n_q < 0 || n_q > h->cfg.max_query_tokens) return KVC_ERR_INVALID_ARG;
-  if (n_q > 0 && (!Q || !out || !aligned16(Q) || !aligned16(out))) return KVC_ERR_INVALID_ARG;
-  // The plan is valid for this block only if its pages are the planned ones.
-  const Block& b = h->blocks[block];
-  if (b.scale.size != h->plan_n_scale || b.live.size != h->plan_n_live ||
-      b.special_frames != h->plan_special_frames)
-    return KVC_ERR_STALE_PLAN;
-  for (int32_t i = 0; i < b.scale.size; ++i)
-    if (b.scale.at(i) != h->plan_snapshot[i]) return KVC_ERR_STALE_PLAN;
-  for (int32_t i = 0; i < b.live.size; ++i)
-    if (b.live.at(i) != h->plan_snapshot[b.scale.size + i]) return KVC_ERR_STALE_PLAN;
-  if (n_q == 0) return KVC_OK;
+  int rc = check_run(h, block, Q, out, n_q);
+  if (rc || n_q == 0) return rc;
   const int kernel = h->plan_kernel;
   const int splits = choose_splits(h, kernel, n_q);
-  kvc::AttnArgs a;
-  a.q = Q;
-  a.out = out;
-  a.cache = h->cache + (size_t)block * h->g.block_bytes;
-  a.tiles = (const kvc::KvTile*)(h->ws + h->g.L.tiles);
-  a.part_o = (float*)(h->ws + h->g.L.part_o);
-  a.part_lse = (float*)(h->ws + h->g.L.part_lse);
-  a.status = (int32_t*)(h->ws + h->g.L.status);
-  a.n_q = n_q;
-  a.num_heads = h->cfg.num_heads;
-  a.head_dim = h->cfg.head_dim;
-  a.page_size = h->cfg.page_size;
-  a.n_tiles = h->plan_n_tiles;
-  a.n_splits = splits;
-  a.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
-  a.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
-  a.stall_test = h->stall_test;
+  const kvc::AttnArgs a = attn_args(h, block, Q, out, n_q, splits);
   cudaStream_t st = (cudaStream_t)stream;
   if (h->timing) record_timing(h, 0, st);
-  cudaError_t err = kernel == 2 ? kvc::launch_attn_tc(a, h->maps, block, h->g.max_pages, h->cfg.dtype, st)
-                                : kvc::launch_attn_simt(a, h->cfg.dtype, st);
+  cudaError_t err;
+  if (kernel == 2) {
+    kvc::TcBatchArgs tb = tc_batch_header(h, Q, out, n_q);
+    tb.count = 1;
+    tb.req[0] = tc_request(h, block, 0, n_q, splits);
+    err = kvc::launch_attn_tc(tb, st);
+  } else {
+    err = kvc::launch_attn_simt(a, h->cfg.dtype, st);
+  }
   if (h->timing) record_timing(h, 1, st);
   if (err != cudaSuccess) return KVC_ERR_CUDA;
   ++h->launches;
@@ -519,6 +569,101 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
     err = kvc::launch_merge(a, h->cfg.dtype, st);
     if (err != cudaSuccess) return KVC_ERR_CUDA;
     ++h->launches;
+  }
+  return KVC_OK;
+}
+
+// Several independent streams in one launch: FlashInfer's batch plan takes a
+// qo_indptr with one entry per request ([KVC] "Kernel-Level Execution Flow");
+// the pages only ever use one.  Request r is handle hs[r]'s block blocks[r]
+// with query rows [qo_indptr[r], qo_indptr[r+1]) of Q / out.
+int kvc_run_batch(kvc_handle* const* hs, const int32_t* blocks, int32_t count, const void* Q, void* out,
+                  const int32_t* qo_indptr, kvc_stream stream) {
+  if (!hs || !blocks || !qo_indptr || count < 1 || count > kvc::kTcMaxBatch) return KVC_ERR_INVALID_ARG;
+  if (qo_indptr[0] != 0) return KVC_ERR_INVALID_ARG;
+  for (int32_t r = 0; r < count; ++r) {
+    kvc_handle* h = hs[r];
+    if (!h) return KVC_ERR_INVALID_ARG;
+    if (qo_indptr[r + 1] < qo_indptr[r]) return KVC_ERR_INVALID_ARG;
+    for (int32_t o = 0; o < r; ++o)
+      if (hs[o] == h) return KVC_ERR_INVALID_ARG;   // each handle's partials serve one request
+    const kvc_config& c0 = hs[0]->cfg;
+    if (h->cfg.num_heads != c0.num_heads || h->cfg.head_dim != c0.head_dim || h->cfg.dtype != c0.dtype ||
+        h->cfg.sm_scale != c0.sm_scale)
+      return KVC_ERR_INVALID_ARG;
+  }
+  const int64_t row_bytes = hs[0]->g.row_bytes;
+  const int32_t rows = qo_indptr[count];
+  // Every request checked before anything is launched.
+  bool all_tc = true;
+  for (int32_t r = 0; r < count; ++r) {
+    const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
+    const char* q = n_q ? (const char*)Q + (int64_t)qo_indptr[r] * row_bytes : nullptr;
+    char* o = n_q ? (char*)out + (int64_t)qo_indptr[r] * row_bytes : nullptr;
+    int rc = check_run(hs[r], blocks[r], q, o, n_q);
+    if (rc) return rc;
+    all_tc = all_tc && hs[r]->plan_kernel == 2;
+  }
+  if (rows == 0) return KVC_OK;
+  if (!all_tc) {
+    // No batched CUDA-core kernel: the requests run one after the other.
+    for (int32_t r = 0; r < count; ++r) {
+      const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
+      if (n_q == 0) continue;
+      int rc = kvc_run(hs[r], blocks[r], (const char*)Q + (int64_t)qo_indptr[r] * row_bytes,
+                       (char*)out + (int64_t)qo_indptr[r] * row_bytes, n_q, stream);
+      if (rc) return rc;
+    }
+    return KVC_OK;
+  }
+  // One split count for the whole launch: balance waves of all requests'
+  // CTAs against the largest per-split tile count.
+  kvc_handle* h0 = hs[0];
+  int max_s = 1 << 30, max_tiles = 1;
+  int64_t base = 0;
+  for (int32_t r = 0; r < count; ++r) {
+    const kvc_handle* h = hs[r];
+    const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
+    if (h->cfg.max_kv_splits < max_s) max_s = h->cfg.max_kv_splits;
+    if (h->plan_n_tiles > max_tiles) max_tiles = h->plan_n_tiles;
+    base += (int64_t)((n_q + kvc::kTcQRows - 1) / kvc::kTcQRows) * h->cfg.num_heads;
+  }
+  if (max_s < 1) max_s = 1;
+  int splits = 1;
+  if (h0->opt_splits > 0) {
+    splits = h0->opt_splits < max_s ? h0->opt_splits : max_s;
+  } else {
+    const int64_t slots = h0->num_sms;
+    double best = 1e300;
+    for (int s = 1; s <= max_s; ++s) {
+      const int64_t waves = (base * s + slots - 1) / slots;
+      const int64_t per = (max_tiles + s - 1) / s;
+      const double cost = (double)waves * per * (1.0 + (s > 1 ? 0.02 * s : 0.0));
+      if (cost < best - 1e-9) { best = cost; splits = s; }
+    }
+  }
+  kvc::TcBatchArgs tb = tc_batch_header(h0, Q, out, rows);
+  tb.count = count;
+  for (int32_t r = 0; r < count; ++r) {
+    const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
+    const int s_r = splits < hs[r]->plan_n_tiles ? splits : hs[r]->plan_n_tiles;
+    tb.req[r] = tc_request(hs[r], blocks[r], qo_indptr[r], n_q, s_r > 0 ? s_r : 1);
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h0->timing) record_timing(h0, 0, st);
+  cudaError_t err = kvc::launch_attn_tc(tb, st);
+  if (h0->timing) record_timing(h0, 1, st);
+  if (err != cudaSuccess) return KVC_ERR_CUDA;
+  ++h0->launches;
+  ++h0->attn_launches;
+  for (int32_t r = 0; r < count; ++r) {
+    if (tb.req[r].n_splits <= 1 || tb.req[r].n_q == 0) continue;
+    const int32_t n_q = tb.req[r].n_q;
+    const kvc::AttnArgs a = attn_args(hs[r], blocks[r], (const char*)Q + (int64_t)qo_indptr[r] * row_bytes,
+                                      (char*)out + (int64_t)qo_indptr[r] * row_bytes, n_q, tb.req[r].n_splits);
+    err = kvc::launch_merge(a, hs[r]->cfg.dtype, st);
+    if (err != cudaSuccess) return KVC_ERR_CUDA;
+    ++h0->launches;
   }
   return KVC_OK;
 }

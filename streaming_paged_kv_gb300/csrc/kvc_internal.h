@@ -89,7 +89,27 @@ struct TcMaps;   // opaque: TMA descriptors of the cache (per handle)
 TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, int page_size,
                        int num_heads, int head_dim, cudaError_t* err);
 void tc_destroy_maps(TcMaps* m);
-cudaError_t launch_attn_tc(const AttnArgs& a, TcMaps* maps, int block, int max_pages, int dtype,
-                           cudaStream_t stream);
+// One tensor-core launch over up to kTcMaxBatch requests (independent streams,
+// each with its own cache, plan and partials).  Q and out are one ragged
+// tensor [rows, H, D]; request r owns rows [q_row0, q_row0 + n_q).
+constexpr int kTcMaxBatch = 16;
+struct TcRequestDesc {
+  TcMaps* maps;
+  int32_t block, max_pages;
+  const KvTile* tiles;
+  float* part_o;          // [n_splits][n_q][H][D] (n_splits > 1)
+  float* part_lse;        // [n_splits][n_q][H]
+  int32_t* status;
+  int32_t n_tiles, n_splits, q_row0, n_q;
+};
+struct TcBatchArgs {
+  const void* q;
+  void* out;
+  int32_t rows, num_heads, head_dim, dtype, stall_test, count;
+  float sm_scale_log2;
+  long long wait_budget;
+  TcRequestDesc req[kTcMaxBatch];
+};
+cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream);
 
 }  // namespace kvc

@@ -73,6 +73,7 @@ _SIGS = {
     "kvc_plan": [_P, _P],
     "kvc_run": [_P, _I32, _P, _P, _I32, _P],
     "kvc_prefill": [_P, _I32, _P, _P, _P, _I32, _P, _P],
+    "kvc_run_batch": [ctypes.POINTER(_P), _PI32, _I32, _P, _P, _PI32, _P],
     "kvc_get_cache_stats": [_P, _I32, ctypes.POINTER(kvc_stats)],
     "kvc_get_plan": [_P, _PI32, _PI32, _I32, _PI32, _PI32],
     "kvc_get_deques": [_P, _I32, _PI32, _PI32, _PI32, _PI32, _PI32, _PI32],
@@ -161,6 +162,28 @@ def kvc_run(h, block, q_ptr, out_ptr, n_q, stream=None):
 
 def kvc_prefill(h, block, q_ptr, k_ptr, v_ptr, n_frames, out_ptr, stream=None):
     return _check(lib.kvc_prefill(h, block, q_ptr, k_ptr, v_ptr, n_frames, out_ptr, stream), "kvc_prefill")
+
+
+def kvc_run_batch(handles, blocks, q_ptr, out_ptr, qo_indptr, stream=None):
+    n = len(handles)
+    hs = (_P * n)(*handles)
+    bl = (ctypes.c_int32 * n)(*blocks)
+    qi = (ctypes.c_int32 * (n + 1))(*qo_indptr)
+    return _check(lib.kvc_run_batch(hs, bl, n, q_ptr, out_ptr, qi, stream), "kvc_run_batch")
+
+
+def run_batch(caches, blocks, q, out, rows):
+    """Attention of several streams in one launch: request r is caches[r]
+    (a PagedKVCache) block blocks[r] with the next rows[r] rows of the ragged
+    q / out ([sum(rows), H, D]).  Returns out."""
+    qo = [0]
+    for n in rows:
+        qo.append(qo[-1] + int(n))
+    if len(rows) != len(caches) or qo[-1] != q.shape[0] or out.shape != q.shape:
+        raise ValueError("rows must give one count per cache and add up to q's length")
+    kvc_run_batch([c.h for c in caches], blocks, caches[0]._ptr(q), caches[0]._ptr(out), qo,
+                  caches[0]._stream())
+    return out
 
 
 def kvc_get_cache_stats(h, block):
