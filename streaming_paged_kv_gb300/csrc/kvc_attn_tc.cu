@@ -33,10 +33,11 @@
 // O0 [384,448), O1 [448,512).
 // Q and K/V tiles use the 128-byte swizzle that both TMA and the tensor core
 // understand.  Scores live in the log2 domain (scaled by sm_scale * log2 e).
-// Each row keeps a reference max m_ref; a tile whose row max exceeds it by
-// more than 8 (a factor 256) moves it to that max, and O and the row sum are
-// rescaled (O only after the previous P V product has completed).  Otherwise
-// P is taken against the stale reference, so every P value is at most 2^8.
+// Each row keeps a reference m_ref and takes P against it.  The reference
+// moves (to the tile's row max; O and the row sum are rescaled, O only after
+// the previous P V product has completed) only when a tile's row sum would
+// exceed 2^64: the relative precision of P, O and the sums does not depend on
+// the reference, only their range does, so most tiles need no row max at all.
 //
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
 // the fact in the status word, raises a CTA-wide abort flag, and every role
@@ -85,7 +86,6 @@ constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t buf_col(int b) { return b * BN; }
 __host__ __device__ constexpr uint32_t o_col(int i) { return NBUF * BN + i * HD; }
 static_assert(o_col(QT) <= TMEM_COLS, "TMEM budget");
-constexpr float RESCALE_THRESHOLD = 8.0f;            // log2 units
 constexpr long long kDrainBudget = 1LL << 26;        // cycles for draining after an abort
 
 // Shared memory map (offsets from a 1024-aligned base).
@@ -352,6 +352,12 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
 }
 
 // ------------------------------------------------------------------ kernel
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_st16_at(uint32_t taddr, const uint32_t (&v)[N]) {
+  static_assert(OFF + 16 <= N, "range");
+  tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(&v[OFF]));
+}
+
 // 32 consecutive TMEM columns of this thread's lane into v[off, off + 32).
 template <int OFF, int N>
 __device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&v)[N]) {
@@ -631,55 +637,77 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
-      // Row max of the tile (four independent chains), in log2 units.
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < BN; c += 8) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          m4[u] = fmax3(m4[u], __uint_as_float(v[c + 2 * u]), __uint_as_float(v[c + 2 * u + 1]));
-      }
-      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-      const bool moved = mt > m_ref + RESCALE_THRESHOLD;
-      const float m_use = moved ? mt : m_ref;
-      const float alpha = moved ? ex2(m_ref - m_use) : 1.f;   // 0 while nothing has been accumulated
-      // P = 2^(s * scale - m_use) <= 2^8, packed in pairs over S's first 64 columns.
-      const uint64_t negm2 = f2_pack(-m_use, -m_use);
+      // P = 2^(s * scale - m_ref) against the running reference, held in
+      // registers until the row sum shows that it is usable.  The reference
+      // only has to keep P and the sums finite -- their relative precision
+      // does not depend on it -- so a tile's own max is needed only when its
+      // row sum exceeds 2^64 or is not a number: on the first tile (reference
+      // -inf) and after a jump of about 57 or more in log2 units.
+      uint32_t pk[BN / 2];
       uint64_t ta = 0, tb = 0;
+      auto exponentiate = [&](float m) {
+        const uint64_t negm2 = f2_pack(-m, -m);
+        ta = tb = 0;
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int e = c * 32 + 2 * t;
-          const uint64_t x = ffma2(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl2x2, negm2);
+        for (int t = 0; t < BN / 2; ++t) {
+          const uint64_t x = ffma2(f2_pack(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1])), sl2x2, negm2);
           const float p0 = ex2(f2_lo(x)), p1 = ex2(f2_hi(x));
           if (t & 1) tb = fadd2(tb, f2_pack(p0, p1));
           else ta = fadd2(ta, f2_pack(p0, p1));
           pk[t] = pack2<BF16>(p0, p1);
         }
-        tmem_st16(S_ + c * 16, pk);
-      }
-      if (__any_sync(0xffffffffu, moved) && j > 0) {
-        // Rare: rescale O once the previous P V product into it has completed.
-        ok = wait_bar_warp(g, &o_done[2 * qi + ((j - 1) & 1)], ((j - 1) >> 1) & 1, 8);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < HD / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(O_ + cc * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
+      };
+      exponentiate(m_ref);
+      const float tsum = (f2_lo(ta) + f2_hi(ta)) + (f2_lo(tb) + f2_hi(tb));
+      const bool moved = !(tsum <= 0x1p64f);
+      float alpha = 1.f;
+      if (__any_sync(0xffffffffu, moved)) {
+        // Rare: S is still intact in TMEM (P is stored below).  Reread it, move
+        // the reference of the overflowing rows to their max, redo P, and
+        // rescale O (once the previous P V product has completed) and the sums.
+        tmem_ld32_at<0>(S_, v);
+        tmem_ld32_at<32>(S_ + 32, v);
+        tmem_ld32_at<64>(S_ + 64, v);
+        tmem_ld32_at<96>(S_ + 96, v);
+        tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-          tmem_st32(O_ + cc * 32, o);
+        for (int c = 0; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < BN; c += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            m4[u] = fmax3(m4[u], __uint_as_float(v[c + 2 * u]), __uint_as_float(v[c + 2 * u + 1]));
         }
+        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+        const float m_new = moved ? mt : m_ref;
+        alpha = ex2(m_ref - m_new);                  // 0 while nothing has been accumulated
+        exponentiate(m_new);
+        if (j > 0) {
+          ok = wait_bar_warp(g, &o_done[2 * qi + ((j - 1) & 1)], ((j - 1) >> 1) & 1, 8);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(O_ + cc * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+            tmem_st32(O_ + cc * 32, o);
+          }
+        }
+        m_ref = m_new;
       }
+      // P as 16-bit pairs over S's first 64 columns.
+      tmem_st16_at<0>(S_, pk);
+      tmem_st16_at<16>(S_ + 16, pk);
+      tmem_st16_at<32>(S_ + 32, pk);
+      tmem_st16_at<48>(S_ + 48, pk);
       const uint64_t alpha2 = f2_pack(alpha, alpha);
       la = ffma2(la, alpha2, ta);
       lb = ffma2(lb, alpha2, tb);
-      m_ref = m_use;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[b]);                       // P(k) is in TMEM (and O_i rescaled)
