@@ -93,7 +93,9 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + QT * Q_BYTES;
 constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + STAGES * TILE_BYTES;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
+// Dual-mode hand-off from softmax group 1 to group 0: [128 rows][max, sum, flag].
+constexpr uint32_t OFF_XCH = OFF_BAR + 256;
+constexpr uint32_t SMEM_BYTES = OFF_XCH + BM * 3 * 4 + 1024;  // + alignment slack
 
 // ------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -276,6 +278,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
+// Named barrier over the eight softmax warps.
+__device__ __forceinline__ void softmax_sync(int id) {
+  asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
+}
+
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
@@ -381,7 +388,8 @@ struct TcLaunch {
   CUtensorMap q_map;       // [rows, H * D] over every request's query rows
   CUtensorMap cache_map[kTcMaxBatch];   // 3D view of each request's whole cache
   void* out;               // [rows, H, D]
-  int32_t count, num_heads, stall_test, pad;
+  int32_t count, num_heads, stall_test;
+  int32_t allow_dual;      // single-query-tile CTAs may use dual mode (three or more waves of CTAs)
   float sm_scale_log2;
   long long wait_budget;
   TcRequest req[kTcMaxBatch];
@@ -431,7 +439,14 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
   const int t0 = (int)(((int64_t)split * R.n_tiles) / R.n_splits);
   const int t1 = (int)(((int64_t)(split + 1) * R.n_tiles) / R.n_splits);
   const int n = t1 - t0;
-  const int n_s = n * nq;                         // score tiles of this CTA
+  // Dual mode: a CTA with a single query tile lets both softmax groups work
+  // on it, each on every other KV tile and with its own O accumulator; group
+  // 0 combines the two halves at the end.  Measured, it pays when CTAs queue
+  // for SMs in three or more waves, and costs a few percent in one or two.
+  const bool dual = P.allow_dual && !has_q1 && n >= 2;
+  const int groups = (has_q1 || dual) ? 2 : 1;    // active softmax groups
+  const int per_tile = dual ? 1 : nq;             // score tiles per KV tile
+  const int n_s = n * per_tile;                   // score tiles of this CTA
   const KvTile* tiles = R.tiles;
   const CUtensorMap* cache_map = &P.cache_map[rq];
   Guard g{abort_flag, R.status, P.wait_budget};
@@ -534,18 +549,18 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
           if (!ok) break;
           tc_fence_after();
           const uint64_t dK = dK0 + (uint64_t)st * STAGE_STEP;
-          const uint64_t dQ = dQ0 + (uint64_t)i * Q_STEP;
+          const uint64_t dQ = dQ0 + (uint64_t)(dual ? 0 : i) * Q_STEP;
           const uint32_t d = tmem + buf_col(b);
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
               umma(d, dQ + kk * K16_STEP, dK + kk * K16_STEP, IDESC_S, kk > 0);
             umma_commit(&s_full[b]);
-            if (i == nq - 1) umma_commit(&kv_empty[st]);
+            if (i == per_tile - 1) umma_commit(&kv_empty[st]);
           }
           __syncwarp();
           b = b == NBUF - 1 ? 0 : b + 1;
-          if (++i == nq) {
+          if (++i == per_tile) {
             i = 0;
             st = st == STAGES - 1 ? 0 : st + 1;
           }
@@ -571,18 +586,22 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
           if (!ok) break;
           tc_fence_after();
           const uint64_t dV = dV0 + (uint64_t)st * STAGE_STEP;
-          const uint32_t o = tmem + o_col(i), pa = tmem + buf_col(b);
+          // The O accumulator this score tile goes to, and how many tiles
+          // that accumulator has taken before.
+          const int grp = dual ? (k & 1) : i;
+          const int jg = dual ? (k >> 1) : j;
+          const uint32_t o = tmem + o_col(grp), pa = tmem + buf_col(b);
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              umma_ts(o, pa + kk * 8, dV + kk * V16_STEP, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+              umma_ts(o, pa + kk * 8, dV + kk * V16_STEP, IDESC_O, (jg > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&buf_free[b]);
-            umma_commit(&o_done[2 * i + (j & 1)]);
-            if (i == nq - 1) umma_commit(&kv_empty[st]);
+            umma_commit(&o_done[2 * grp + (jg & 1)]);
+            if (i == per_tile - 1) umma_commit(&kv_empty[st]);
           }
           __syncwarp();
           b = b == NBUF - 1 ? 0 : b + 1;
-          if (++i == nq) {
+          if (++i == per_tile) {
             i = 0;
             ++j;
             st = st == STAGES - 1 ? 0 : st + 1;
@@ -608,13 +627,16 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     float m_ref = -INFINITY;
     uint64_t la = 0, lb = 0;                         // row-sum partials (two fp32 pairs)
-    bool ok = n > 0 && qi < nq;                      // warp-uniform
+    bool ok = n > 0 && qi < groups;                  // warp-uniform
+    // This group's tiles: j counts them; in dual mode the group takes KV
+    // tiles qi, qi + 2, ..., otherwise every KV tile.
+    const int n_g = dual ? (n - qi + 1) / 2 : n;
 
-    int rows_next = ok ? tiles[t0].rows : 0;
-    for (int j = 0; ok && j < n; ++j) {
-      const int k = j * nq + qi, b = k % NBUF;
+    int rows_next = ok ? tiles[t0 + (dual ? qi : 0)].rows : 0;
+    for (int j = 0; ok && j < n_g; ++j) {
+      const int k = j * groups + qi, b = k % NBUF;
       const int rows_valid = rows_next;
-      if (j + 1 < n) rows_next = tiles[t0 + j + 1].rows;   // prefetch for the next tile
+      if (j + 1 < n_g) rows_next = tiles[t0 + (dual ? k + 2 : j + 1)].rows;   // prefetch for the next tile
       ok = wait_bar_warp(g, &s_full[b], (k / NBUF) & 1, 6);
       if (!ok) break;
       tc_fence_after();
@@ -712,11 +734,37 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
       tc_fence_before();
       mbar_arrive(&p_full[b]);                       // P(k) is in TMEM (and O_i rescaled)
     }
-    if (n > 0 && qi < nq) {
-      // Epilogue: wait for the last P V product, normalise, write the row.
-      const bool good = ok && wait_bar_warp(g, &o_done[2 * qi + ((n - 1) & 1)], ((n - 1) >> 1) & 1, 9);
+    if (n > 0 && qi < groups) {
+      // Epilogue: wait for this group's last P V product, normalise, write
+      // the row.  In dual mode group 1 hands its row max and sum to group 0
+      // through shared memory, and group 0 combines both halves (group 1's O
+      // sits in the same TMEM lanes) before writing.
+      bool good = ok && wait_bar_warp(g, &o_done[2 * qi + ((n_g - 1) & 1)], ((n_g - 1) >> 1) & 1, 9);
+      float l = (f2_lo(la) + f2_hi(la)) + (f2_lo(lb) + f2_hi(lb));
+      float m_fin = m_ref, w0 = 1.f, w1 = 0.f;
+      if (dual) {
+        float* xr = reinterpret_cast<float*>(smem + OFF_XCH) + 3 * r;
+        if (qi == 1) {
+          xr[0] = m_ref;
+          xr[1] = l;
+          xr[2] = good ? 0.f : 1.f;
+        }
+        softmax_sync(2);
+        if (qi == 1) {
+          good = false;                              // group 0 writes the row
+        } else if (good && xr[2] == 0.f) {
+          const int n_g1 = n / 2;                    // group 1's tiles
+          good = wait_bar_warp(g, &o_done[2 + ((n_g1 - 1) & 1)], ((n_g1 - 1) >> 1) & 1, 9);
+          const float m1 = xr[0], l1 = xr[1];
+          m_fin = fmaxf(m_ref, m1);
+          w0 = ex2(m_ref - m_fin);
+          w1 = ex2(m1 - m_fin);
+          l = w0 * l + w1 * l1;
+        } else {
+          good = false;
+        }
+      }
       if (good) {
-        const float l = (f2_lo(la) + f2_hi(la)) + (f2_lo(lb) + f2_hi(lb));
         tc_fence_after();
         uint32_t v[HD];
         tmem_ld32_at<0>(O_, v);
@@ -724,6 +772,16 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < HD; ++c) asm volatile("" : "+r"(v[c])::"memory");
+        if (dual) {
+          uint32_t v1[HD];
+          const uint32_t O1 = lane_base + o_col(1);
+          tmem_ld32_at<0>(O1, v1);
+          tmem_ld32_at<32>(O1 + 32, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < HD; ++c)
+            v[c] = __float_as_uint(fmaf(w1, __uint_as_float(v1[c]), w0 * __uint_as_float(v[c])));
+        }
         const int row = q0 + qi * BM + r;             // within the request
         if (row < R.n_q) {
           const float inv = 1.f / l;
@@ -747,7 +805,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
             for (int i = 0; i < HD / 4; ++i)
               dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
                                    __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
-            R.part_lse[((int64_t)split * R.n_q + row) * P.num_heads + h] = m_ref + __log2f(l);
+            R.part_lse[((int64_t)split * R.n_q + row) * P.num_heads + h] = m_fin + __log2f(l);
           }
         }
       }
@@ -868,6 +926,7 @@ cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
     ctas += (int64_t)q.q_blocks * b.num_heads * d.n_splits;
   }
   if (ctas == 0) return cudaSuccess;
+  P.allow_dual = ctas > 2 * (int64_t)b.num_sms ? 1 : 0;   // measured: helps from about three waves on
   if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
   const int which = b.dtype == 0 ? 0 : 1;
   auto kernel = which == 0 ? attn_tc_kernel<true> : attn_tc_kernel<false>;

@@ -303,6 +303,7 @@ kvc::TcBatchArgs tc_batch_header(const kvc_handle* h, const void* Q, void* out, 
   tb.head_dim = h->cfg.head_dim;
   tb.dtype = h->cfg.dtype;
   tb.stall_test = h->stall_test;
+  tb.num_sms = h->num_sms;
   tb.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
   tb.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
   return tb;

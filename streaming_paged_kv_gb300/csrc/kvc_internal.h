@@ -106,6 +106,7 @@ struct TcBatchArgs {
   const void* q;
   void* out;
   int32_t rows, num_heads, head_dim, dtype, stall_test, count;
+  int32_t num_sms;        // of the device: decides whether a launch has several waves
   float sm_scale_log2;
   long long wait_budget;
   TcRequestDesc req[kTcMaxBatch];
