@@ -625,7 +625,9 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
     const uint32_t O_ = lane_base + o_col(qi);
     const float sl2 = P.sm_scale_log2;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    float m_ref = -INFINITY;
+    // Starting reference: any finite value within a few tens of the scores
+    // (log2 units) works, so ordinary first tiles need no row max either.
+    float m_ref = 0.f;
     uint64_t la = 0, lb = 0;                         // row-sum partials (two fp32 pairs)
     bool ok = n > 0 && qi < groups;                  // warp-uniform
     // This group's tiles: j counts them; in dual mode the group takes KV
@@ -663,8 +665,8 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
       // registers until the row sum shows that it is usable.  The reference
       // only has to keep P and the sums finite -- their relative precision
       // does not depend on it -- so a tile's own max is needed only when its
-      // row sum exceeds 2^64 or is not a number: on the first tile (reference
-      // -inf) and after a jump of about 57 or more in log2 units.
+      // row sum exceeds 2^64 or is not a number (after a jump of about 57 or
+      // more in log2 units), or -- on the first tile -- falls below 2^-64.
       uint32_t pk[BN / 2];
       uint64_t ta = 0, tb = 0;
       auto exponentiate = [&](float m) {
@@ -681,7 +683,8 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
       };
       exponentiate(m_ref);
       const float tsum = (f2_lo(ta) + f2_hi(ta)) + (f2_lo(tb) + f2_hi(tb));
-      const bool moved = !(tsum <= 0x1p64f);
+      // The first tile also moves the reference when its sum underflows.
+      const bool moved = !(tsum <= 0x1p64f) || (j == 0 && !(tsum >= 0x1p-64f));
       float alpha = 1.f;
       if (__any_sync(0xffffffffu, moved)) {
         // Rare: S is still intact in TMEM (P is stored below).  Reread it, move
@@ -703,7 +706,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
         }
         const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
         const float m_new = moved ? mt : m_ref;
-        alpha = ex2(m_ref - m_new);                  // 0 while nothing has been accumulated
+        alpha = j > 0 ? ex2(m_ref - m_new) : 0.f;    // nothing accumulated before the first tile
         exponentiate(m_new);
         if (j > 0) {
           ok = wait_bar_warp(g, &o_done[2 * qi + ((j - 1) & 1)], ((j - 1) >> 1) & 1, 8);
