@@ -525,7 +525,8 @@ def run_batch224(args, rank, world):
 def run_e2e(args, kvc, w, dev, rank, world):
     """The same frames/s through the public API with host inputs: every step
     copies that frame's Q/K/V of every layer from pinned host memory and reads
-    every layer's output back to pinned host memory inside the timed region."""
+    every layer's output back to pinned host memory inside the timed region
+    (on their own streams, overlapping the attention launches)."""
     import torch
     K = max(1, min(args.e2e_steps, w.n_frames))
     W = min(4, w.n_frames - K)
@@ -537,21 +538,43 @@ def run_e2e(args, kvc, w, dev, rank, world):
     host = [[torch.randn(T, H, D, generator=g).to(torch.bfloat16).pin_memory() for _ in range(3)]
             for _ in range(L)]
     host_out = [torch.empty(T, H, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
-    dq = [torch.empty(T, H, D, dtype=torch.bfloat16, device=dev) for _ in range(3)]
-    dout = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    # Copies overlap the attention: inputs go up on one stream and outputs
+    # come back on another, into double-buffered device tensors; events order
+    # each buffer's reuse after the launch that read or wrote it.
+    comp = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dq = [[torch.empty(T, H, D, dtype=torch.bfloat16, device=dev) for _ in range(3)] for _ in range(2)]
+    dout = [torch.empty(T, H, D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    fetched = [torch.cuda.Event() for _ in range(2)]
+    for e in consumed + fetched:
+        e.record(comp)
+    seq = [0]
 
     def frame(attend=True):
         for b in range(L):
-            for i in range(3):
-                dq[i].copy_(host[b][i], non_blocking=True)
-            c.append_frame(b, dq[1], dq[2])
+            p = seq[0] & 1
+            seq[0] += 1
+            with torch.cuda.stream(up):
+                up.wait_event(consumed[p])           # the launch that last read dq[p] is done
+                for i in range(3):
+                    dq[p][i].copy_(host[b][i], non_blocking=True)
+                uploaded[p].record(up)
+            comp.wait_event(uploaded[p])
+            c.append_frame(b, dq[p][1], dq[p][2])
             c.evict_frames(b)
-            if not attend:
-                continue
-            if b == 0:
-                c.plan()
-            c.run(b, dq[0], dout)
-            host_out[b].copy_(dout, non_blocking=True)
+            if attend:
+                if b == 0:
+                    c.plan()
+                comp.wait_event(fetched[p])          # dout[p] has been copied back
+                c.run(b, dq[p][0], dout[p])
+            consumed[p].record(comp)
+            if attend:
+                with torch.cuda.stream(down):
+                    down.wait_event(consumed[p])
+                    host_out[b].copy_(dout[p], non_blocking=True)
+                    fetched[p].record(down)
 
     for _ in range(w.n_frames - K - W):
         frame(attend=False)
