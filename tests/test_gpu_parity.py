@@ -219,3 +219,33 @@ def test_max_jumps_inside_and_across_tiles(kvc, kernel):
     torch.cuda.synchronize()
     mx, rel = compare(out, want, "bf16")
     assert mx <= 2e-2 and rel <= 5e-3, (mx, rel)
+
+
+# ------------------------------------------------------- dtypes / head sizes
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_f16_stream(kvc, kernel):
+    """fp16 caches: the tensor-core kernel's fp16 instantiation (P packed as
+    fp16) and the CUDA-core kernel, through the first eviction, with splits."""
+    w = WORKLOADS["s224"].with_(num_layers=1, n_frames=80, dtype="f16")
+    _kernel_or_skip(kvc, w, kernel)
+    e = ParityEngine(kvc, w, check_frames={0, 9, 40, 72, 79}, kernel=kernel, check_bytes=False)
+    drive(w, e)
+    mx, rel = e.worst()
+    assert mx <= TOL["f16"][0] and rel <= TOL["f16"][1], e.results
+    e.close()
+
+
+@pytest.mark.parametrize("head_dim", [32, 128])
+def test_other_head_sizes_cuda_core(kvc, head_dim):
+    """Head sizes without a tensor-core kernel run on the CUDA cores (bf16)."""
+    w = WORKLOADS["s224"].with_(num_layers=1, n_frames=12, head_dim=head_dim, num_heads=8,
+                                sliding_window=4, headroom=2, max_total_frames=64)
+    e = ParityEngine(kvc, w, check_frames={0, 5, 11})
+    drive(w, e)
+    mx, rel = e.worst()
+    assert mx <= TOL["bf16"][0] and rel <= TOL["bf16"][1], e.results
+    c = e.c
+    # auto kernel selection picked the CUDA-core kernel for this head size
+    with pytest.raises(kvc.KvcError):
+        c.set_option(kvc.KVC_OPT_ATTN_KERNEL, 2)
+    e.close()
