@@ -181,20 +181,31 @@ class Stream:
         return self.w.page_size * (s["scale_pages"] + s["live_pages"]) + s["special_tokens"]
 
 
+def kernel_code_hash(path):
+    """sha256 of a CUDA source with its comments and blank lines removed, so
+    that only a change of code (not of commentary) marks counters as stale."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def profiled_traffic(alg_bytes_per_launch):
     """DRAM bytes per attention launch from the committed ncu summary, scaled to
     this run's average launch by algorithmic bytes -- or None when the kernel
-    source differs from the one the counters were taken on."""
-    import hashlib
+    code differs from the one the counters were taken on."""
     import re
     prof = os.path.join(ROOT, "profiles", "attn_tc_s518_l1f200_full.md")
     src = os.path.join(ROOT, "streaming_paged_kv_gb300", "csrc", "kvc_attn_tc.cu")
     try:
         text = open(prof, encoding="utf-8").read()
-        sha = re.search(r"^kernel_source_sha256: ([0-9a-f]+)$", text, re.M).group(1)
+        sha = re.search(r"^kernel_code_sha256: ([0-9a-f]+)$", text, re.M).group(1)
         dram = float(re.search(r"^dram_bytes_per_launch: (\d+)$", text, re.M).group(1))
         alg = float(re.search(r"^alg_bytes_per_launch: (\d+)$", text, re.M).group(1))
-        if hashlib.sha256(open(src, "rb").read()).hexdigest() != sha:
+        if kernel_code_hash(src) != sha:
             return None
         return dram * alg_bytes_per_launch / alg
     except Exception:

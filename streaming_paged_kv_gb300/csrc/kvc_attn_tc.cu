@@ -15,8 +15,9 @@
 // for Streaming Inference with FlashInfer Integration"; [PERF] "How to Improve
 // Streaming Inference Performance with FlashInfer KV Cache Backend".
 //
-// CTA = two 128-row query tiles (Q0, Q1) x one head x one KV split; each K/V
-// tile is loaded once and serves both query tiles.  Warps:
+// A launch serves up to kTcMaxBatch independent requests (streams); a CTA =
+// two 128-row query tiles (Q0, Q1) of one request x one head x one KV split;
+// each K/V tile is loaded once and serves both query tiles.  Warps:
 //   0-3   softmax + epilogue of Q0, 4-7 softmax + epilogue of Q1: one thread
 //         per query row (warp w owns TMEM lanes [32(w%4), +32)), holding the
 //         row's 128 scores of a tile in registers
@@ -30,14 +31,16 @@
 // S(k+3) may enter buffer b once P(k) V has completed, so while one query
 // tile's warps exponentiate, the other tile's next scores are already being
 // computed.  TMEM (512 columns): buffers [0,128) [128,256) [256,384),
-// O0 [384,448), O1 [448,512).
+// O0 [384,448), O1 [448,512).  A CTA with a single query tile may run in dual
+// mode (below): then both warp groups share Q0, taking alternate KV tiles.
 // Q and K/V tiles use the 128-byte swizzle that both TMA and the tensor core
 // understand.  Scores live in the log2 domain (scaled by sm_scale * log2 e).
-// Each row keeps a reference m_ref and takes P against it.  The reference
-// moves (to the tile's row max; O and the row sum are rescaled, O only after
-// the previous P V product has completed) only when a tile's row sum would
-// exceed 2^64: the relative precision of P, O and the sums does not depend on
-// the reference, only their range does, so most tiles need no row max at all.
+// Each row keeps a reference m_ref, starting at 0, and takes P against it.
+// The reference moves (to the tile's row max; O and the row sum are rescaled,
+// O only after the previous P V product has completed) only when a tile's row
+// sum would exceed 2^64 (or, on the first tile, fall below 2^-64): the
+// relative precision of P, O and the sums does not depend on the reference,
+// only their range does, so most tiles need no row max at all.
 //
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
 // the fact in the status word, raises a CTA-wide abort flag, and every role
