@@ -208,27 +208,36 @@ __global__ void merge_kernel(const AttnArgs a) {
   const float* lse = a.part_lse + rh;
   const float4* po = reinterpret_cast<const float4*>(a.part_o + rh * D) + c;
   const int64_t po_stride = n_rh * (D / 4);
-  float mx = -INFINITY;
-#pragma unroll 8
-  for (int s = 0; s < a.n_splits; ++s) mx = fmaxf(mx, __ldg(lse + s * n_rh));
-  float wsum = 0.f;
+  // One pass with a running max: each split's weight and partial are loaded
+  // together, so the unrolled loop keeps several splits' loads in flight.
+  float mx = -INFINITY, wsum = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
   for (int s = 0; s < a.n_splits; ++s) {
-    const float wt = exp2f(__ldg(lse + s * n_rh) - mx);
+    const float l_s = __ldg(lse + s * n_rh);
     const float4 p = __ldg(po + s * po_stride);
-    wsum += wt;
-    o.x = fmaf(wt, p.x, o.x);
-    o.y = fmaf(wt, p.y, o.y);
-    o.z = fmaf(wt, p.z, o.z);
-    o.w = fmaf(wt, p.w, o.w);
+    const float m_new = fmaxf(mx, l_s);
+    const float scale = exp2f(mx - m_new);         // 0 on the first split
+    const float wt = exp2f(l_s - m_new);
+    mx = m_new;
+    wsum = fmaf(wsum, scale, wt);
+    o.x = fmaf(wt, p.x, o.x * scale);
+    o.y = fmaf(wt, p.y, o.y * scale);
+    o.z = fmaf(wt, p.z, o.z * scale);
+    o.w = fmaf(wt, p.w, o.w * scale);
   }
   const float inv = 1.f / wsum;
   T* op = reinterpret_cast<T*>(a.out) + rh * D + 4 * c;
-  op[0] = from_f<T>(o.x * inv);
-  op[1] = from_f<T>(o.y * inv);
-  op[2] = from_f<T>(o.z * inv);
-  op[3] = from_f<T>(o.w * inv);
+  if constexpr (sizeof(T) == 2) {                    // one 8-byte store
+    union { T t[4]; uint2 u; } w;
+    w.t[0] = from_f<T>(o.x * inv);
+    w.t[1] = from_f<T>(o.y * inv);
+    w.t[2] = from_f<T>(o.z * inv);
+    w.t[3] = from_f<T>(o.w * inv);
+    *reinterpret_cast<uint2*>(op) = w.u;
+  } else {
+    *reinterpret_cast<float4*>(op) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+  }
 }
 
 template <typename T, int D>
