@@ -45,6 +45,7 @@ def parse():
     p.add_argument("--workload", default="s518",
                    help="s518 (default, the streamed metric), another streaming workload, phase1 or batch224")
     p.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
+    p.add_argument("--splits", type=int, default=0, help="tuning: force the KV split count (0 = the library's choice)")
     p.add_argument("--pool", type=int, default=4, help="distinct input frames per layer")
     p.add_argument("--batch", type=int, default=8, help="streams of --workload batch224")
     p.add_argument("--seed", type=int, default=0)
@@ -123,7 +124,7 @@ class ClockSampler:
 class Stream:
     """One device stream of the workload through the library."""
 
-    def __init__(self, kvc, w, pool, seed, kernel, dev):
+    def __init__(self, kvc, w, pool, seed, kernel, dev, splits=0):
         import torch
         from streaming_paged_kv_gb300.inputs import k_head_scale
         self.torch, self.kvc, self.w = torch, kvc, w
@@ -132,6 +133,8 @@ class Stream:
                                   device=dev)
         if kernel:
             self.c.set_option(kvc.KVC_OPT_ATTN_KERNEL, kernel)
+        if splits:
+            self.c.set_option(kvc.KVC_OPT_NUM_SPLITS, splits)
         T, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
@@ -248,7 +251,7 @@ def run_ours(args, rank, world):
     W = args.warmup
     K = max(1, min(K, w.n_frames))
     W = max(0, min(W, w.n_frames - K))
-    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev)
+    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits)
     st.fast_forward(w.n_frames - K - W)
     for _ in range(W):
         st.step()
