@@ -43,7 +43,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="s518",
-                   help="s518 (default, the streamed metric), another streaming workload, phase1 or batch224")
+                   help="s518 (default, the streamed metric), s224, phase1, batch224 or win518")
     p.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     p.add_argument("--splits", type=int, default=0, help="tuning: force the KV split count (0 = the library's choice)")
     p.add_argument("--pool", type=int, default=4, help="distinct input frames per layer")
@@ -334,6 +334,139 @@ def run_ours(args, rank, world):
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, kvc, w, dev, rank, world)
     return res
+
+
+WINDOW_METRIC = ("windowed-stream frames/s (518x378, 24-layer paged attn, 128-slot window reset per window, "
+                 "keyframe interval 13); attn TFLOP/s vs GB300 roofline")
+
+
+def run_windowed(args, rank, world):
+    """The windowed long stream: a window of 8 scale + 120 keyframe slots,
+    reset with clean at its start; one frame in 13 after the scale frames is
+    a keyframe (append, evict, plan, attend), the others attend over the cache
+    plus themselves and are rolled back.  Timed: one whole window from a clean
+    start, after warm-up frames of a first window; frames/s and the device
+    time of every frame (p50 / p99)."""
+    import torch
+    from streaming_paged_kv_gb300 import build
+    build.build()
+    from streaming_paged_kv_gb300 import kvc
+    from streaming_paged_kv_gb300.workloads import WORKLOADS, schedule
+    w = WORKLOADS["win518"]
+    if args.layers:
+        w = w.with_(num_layers=args.layers)
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    K = min(args.steps or w.window_frames, w.window_frames)
+    W = max(args.warmup, 3)
+    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits)
+    c, L = st.c, w.num_layers
+    book = kvc.PagedKVCache(1, w.num_heads, w.head_dim, w.page_size, w.dtype, w.scale_frames,
+                            w.sliding_window, w.headroom, w.max_total_frames, device=None)
+
+    def frame(f, kind, count=None):
+        if kind == "clean":
+            c.clean()
+            book.clean()
+            return
+        prov = kind == "reject"
+        if prov:
+            c.set_defer_eviction(True)
+            book.set_defer_eviction(True)
+        book.append_frame(0)
+        book.evict_frames(0)
+        if count is not None:
+            s_ = book.stats(0)
+            count.append(w.page_size * (s_["scale_pages"] + s_["live_pages"]) + s_["special_tokens"])
+        for b in range(L):
+            q, k, v = st.inputs(f, b)
+            c.append_frame(b, k, v)
+            c.evict_frames(b)
+            if b == 0:
+                c.plan()
+            c.run(b, q, st.out[b])
+        if prov:
+            for b in range(L):
+                c.rollback_last_frame(b)
+            book.rollback_last_frame(0)
+            c.set_defer_eviction(False)
+            book.set_defer_eviction(False)
+
+    events = schedule(w)
+    done = 0
+    for f, kind in events:                      # warm-up: the first frames of a window
+        frame(f, kind)
+        if kind != "clean":
+            done += 1
+            if done == W:
+                break
+    torch.cuda.synchronize()
+    timed = [(f, kind) for f, kind in schedule(w.with_(n_frames=w.window_frames))][:K + 1]
+    kvc.kvc_get_counters(c.h, reset=True)
+    c.set_option(kvc.KVC_OPT_TIMING, 1)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    nkv = []
+    marks = []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for f, kind in timed:
+        if kind != "clean":
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            marks.append(e)
+        frame(f, kind, nkv)
+    ev1.record()
+    marks.append(ev1)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    n_frames = len(nkv)
+    ms, total_frames = aggregate(ev0.elapsed_time(ev1), n_frames, world, dev)
+    launches, attn_launches, attn_ms = kvc.kvc_get_counters(c.h, reset=True)
+    c.set_option(kvc.KVC_OPT_TIMING, 0)
+    if kvc.kvc_device_status(c.h, c._stream()) != 0:
+        raise RuntimeError("device status")
+    per = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(n_frames))
+    T, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
+    flops = sum(L * 4.0 * T * n * H * D for n in nkv)
+    bytes_alg = sum(L * (2.0 * n * H * D * 2 + 2.0 * T * H * D * 2) for n in nkv)
+    pk = peaks()
+    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
+    book.close()
+    del st
+    torch.cuda.empty_cache()
+    return {
+        "metric": WINDOW_METRIC, "value": total_frames / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
+        "steps": n_frames, "warmup": W, "ms_per_step": ms / n_frames, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"win518: 518x378 windowed stream, {L} layers, H={H}, D={D}, page_size={w.page_size}, "
+                               f"window {w.window_slots} slots ({w.window_frames} frames, keyframe interval "
+                               f"{w.keyframe_interval}); timed = one window from its clean start",
+                   "l2": "no flush: every layer's visible K/V exceeds L2 once the window fills",
+                   "parallelism": f"replicas x{world} (independent streams, no collective)"},
+        "frame_ms": {"p50": per[len(per) // 2], "p99": per[min(len(per) - 1, int(len(per) * 0.99))],
+                     "max": per[-1]},
+        "roofline": {
+            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None, "traffic": None,
+            "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
+            "kernel": "paged attention (kvc_run attention launch)",
+            "flops_per_launch": flops / max(attn_launches, 1),
+            "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
+            "launch_ms": attn_ms / max(attn_launches, 1)},
+        "attn_tflops": achieved,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
 
 
 PHASE1_METRIC = ("Phase-1 batch prefill frames/s (8 scale frames x 1005 tokens, dense bidirectional, "
@@ -736,8 +869,8 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    if args.workload in ("phase1", "batch224"):
-        res = (run_phase1 if args.workload == "phase1" else run_batch224)(args, rank, world)
+    if args.workload in ("phase1", "batch224", "win518"):
+        res = {"phase1": run_phase1, "batch224": run_batch224, "win518": run_windowed}[args.workload](args, rank, world)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if world > 1:
