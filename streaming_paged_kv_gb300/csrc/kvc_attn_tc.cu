@@ -414,17 +414,19 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
   uint64_t* s_full = kv_empty + STAGES;           // [NBUF] S(k) written by the tensor core
   uint64_t* p_full = s_full + NBUF;               // [NBUF] P(k) written (and O rescaled)
   uint64_t* buf_free = p_full + NBUF;             // [NBUF] P(k) V done: the buffer may take S(k+3)
-  // [QT][2] O_i += P_i(j) V(j) done, on barrier [i][j % 2].  Alternating
-  // barriers keep every parity wait unambiguous: when a softmax thread of
-  // tile j waits for P_i(j-1) V, the product of tile j-3 has already
-  // completed and that of tile j+1 has not been issued, so the barrier it
-  // polls is either one phase short of the target or at it.
+  // [QT][3] O_i += P_i(j) V(j) done, on barrier [i][j % 3].  Rotating over
+  // three barriers keeps every parity wait unambiguous: when a softmax
+  // thread waits for product j of its accumulator, product j - 3 (the
+  // barrier's previous phase) has completed -- S of the thread's current
+  // tile waited for the P V product three score tiles back -- and product
+  // j + 3 cannot have been issued, so the barrier it polls is either one
+  // phase short of the target or at it.
   uint64_t* o_done = buf_free + NBUF;
-  uint64_t* drain = o_done + 2 * QT;               // [2] one per MMA-issuing warp
+  uint64_t* drain = o_done + 3 * QT;               // [2] one per MMA-issuing warp
   uint64_t* never = drain + 2;                    // signalled by nothing (timeout test)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  static_assert((1 + 2 * STAGES + 3 * NBUF + 2 * QT + 3) * 8 + 8 <= 256, "barrier area");
+  static_assert((1 + 2 * STAGES + 3 * NBUF + 3 * QT + 3) * 8 + 8 <= 256, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -465,7 +467,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
       mbar_init(&p_full[b], GROUP_THREADS);
       mbar_init(&buf_free[b], 1);
     }
-    for (int i = 0; i < 2 * QT; ++i) mbar_init(&o_done[i], 1);
+    for (int i = 0; i < 3 * QT; ++i) mbar_init(&o_done[i], 1);
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
     mbar_init(never, 1);
@@ -599,7 +601,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
             for (int kk = 0; kk < BN / 16; ++kk)
               umma_ts(o, pa + kk * 8, dV + kk * V16_STEP, IDESC_O, (jg > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&buf_free[b]);
-            umma_commit(&o_done[2 * grp + (jg & 1)]);
+            umma_commit(&o_done[3 * grp + jg % 3]);
             if (i == per_tile - 1) umma_commit(&kv_empty[st]);
           }
           __syncwarp();
@@ -712,7 +714,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
         alpha = j > 0 ? ex2(m_ref - m_new) : 0.f;    // nothing accumulated before the first tile
         exponentiate(m_new);
         if (j > 0) {
-          ok = wait_bar_warp(g, &o_done[2 * qi + ((j - 1) & 1)], ((j - 1) >> 1) & 1, 8);
+          ok = wait_bar_warp(g, &o_done[3 * qi + (j - 1) % 3], ((j - 1) / 3) & 1, 8);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -745,7 +747,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
       // the row.  In dual mode group 1 hands its row max and sum to group 0
       // through shared memory, and group 0 combines both halves (group 1's O
       // sits in the same TMEM lanes) before writing.
-      bool good = ok && wait_bar_warp(g, &o_done[2 * qi + ((n_g - 1) & 1)], ((n_g - 1) >> 1) & 1, 9);
+      bool good = ok && wait_bar_warp(g, &o_done[3 * qi + (n_g - 1) % 3], ((n_g - 1) / 3) & 1, 9);
       float l = (f2_lo(la) + f2_hi(la)) + (f2_lo(lb) + f2_hi(lb));
       float m_fin = m_ref, w0 = 1.f, w1 = 0.f;
       if (dual) {
@@ -760,7 +762,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
           good = false;                              // group 0 writes the row
         } else if (good && xr[2] == 0.f) {
           const int n_g1 = n / 2;                    // group 1's tiles
-          good = wait_bar_warp(g, &o_done[2 + ((n_g1 - 1) & 1)], ((n_g1 - 1) >> 1) & 1, 9);
+          good = wait_bar_warp(g, &o_done[3 + (n_g1 - 1) % 3], ((n_g1 - 1) / 3) & 1, 9);
           const float m1 = xr[0], l1 = xr[1];
           m_fin = fmaxf(m_ref, m1);
           w0 = ex2(m_ref - m_fin);
