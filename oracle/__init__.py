@@ -27,7 +27,7 @@ Pages cited (by tag, then section):
 * [SLOTS] "LingBot-Map KV缓存机制深度揭秘：scale frames与keyframes如何占用slot"
           (mhpq.cn; its sections are the inline headings quoted in Chinese)
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 1. Special packing is frame-aligned: frame s of the stream owns slots
    ``[6*(s % fpp), 6*(s % fpp) + 6)`` of special page ``P + s // fpp`` with

@@ -62,7 +62,8 @@ class OraclePagedKV:
 
     def __init__(self, num_blocks, page_size, num_heads, head_dim, dtype="bf16",
                  scale_frames=8, sliding_window=64, headroom=16,
-                 max_total_frames=2048, mirror_blocks=None):
+                 max_total_frames=2048, mirror_blocks=None,
+                 cross_frame_special=True, camera_only=False):
         if dtype not in _BITS_DTYPE:
             raise ValueError(dtype)
         if page_size < NUM_SPECIAL:
@@ -83,7 +84,24 @@ class OraclePagedKV:
         self.frames_per_special_page = page_size // NUM_SPECIAL
         # The special pool is sized from max_total_frames ([SLOTS] "特殊 token 流").
         self.num_special_pages = -(-max_total_frames // self.frames_per_special_page)
-        self.max_num_pages = self.num_patch_pages + self.num_special_pages
+        # The two eviction options of [KVC] "Streaming Forward Pass" (the block
+        # passes both to evict_frames; the pages never say what they do).
+        # Reading taken: cross_frame_special -- a frame's special tokens stay
+        # visible after its patch page is evicted (the pages' default
+        # behaviour: the special stream is never evicted, [SLOTS] "特殊 token
+        # 流"); with it off they leave the visible set together with the patch
+        # page.  camera_only -- of an evicted frame's specials only the camera
+        # token (the first of the six) stays visible.  The special stream
+        # itself is unchanged (append-only); for camera_only every frame's
+        # camera token is also written to a third append-only stream, the
+        # camera pages, page_size tokens per page, so that the evicted frames'
+        # camera tokens form one contiguous run.
+        self.cross_frame_special = bool(cross_frame_special)
+        self.camera_only = bool(camera_only)
+        self.camera_stream = self.cross_frame_special and self.camera_only
+        self.num_camera_pages = -(-max_total_frames // page_size) if self.camera_stream else 0
+        self.first_camera_page = self.num_patch_pages + self.num_special_pages
+        self.max_num_pages = self.num_patch_pages + self.num_special_pages + self.num_camera_pages
         self.tokens_per_frame = NUM_SPECIAL + page_size
         self.defer_eviction = False
         self.blocks = [_BlockState(self.num_patch_pages) for _ in range(num_blocks)]
@@ -134,22 +152,33 @@ class OraclePagedKV:
             slot = NUM_SPECIAL * (s % self.frames_per_special_page)
             m[sp_page, 0, slot:slot + NUM_SPECIAL] = k_bits[:NUM_SPECIAL]
             m[sp_page, 1, slot:slot + NUM_SPECIAL] = v_bits[:NUM_SPECIAL]
+            if self.camera_stream:
+                # The camera token (row 0) also goes to camera position s.
+                cam_page = self.first_camera_page + s // self.page_size
+                m[cam_page, 0, s % self.page_size] = k_bits[0]
+                m[cam_page, 1, s % self.page_size] = v_bits[0]
         st.special_frames = s + 1
         st.frame_count += 1
         st.undo.append((page, region))
         return page
 
     # ---------------------------------------------------------------- eviction
-    def evict_frames(self, block, scale_frames, sliding_window):
+    def evict_frames(self, block, scale_frames, sliding_window, cross_frame_special=None,
+                     camera_only=None):
         """FIFO eviction of the live window down to ``sliding_window`` pages.
 
-        The oldest live page goes back to the free list; scale pages and
-        special tokens are never evicted ([SLOTS] "keyframes滑动窗口";
-        [KVC] "Append and Evict API").  A no-op while eviction is deferred
-        ([PERF] "Deferred Eviction Strategy").
+        The oldest live page goes back to the free list; scale pages are never
+        evicted, and what stays visible of an evicted frame's special tokens
+        is set by the construction's cross_frame_special / camera_only
+        ([SLOTS] "keyframes滑动窗口"; [KVC] "Append and Evict API",
+        "Streaming Forward Pass").  Passing either option with a value other
+        than the construction's is rejected, like a different scale_frames.
+        A no-op while eviction is deferred ([PERF] "Deferred Eviction
+        Strategy").
         """
         st = self._block(block)
         self._check_scale_arg(scale_frames, sliding_window)
+        self._check_special_args(cross_frame_special, camera_only)
         if self.defer_eviction:
             return 0
         return self._evict(st, sliding_window, commit_always=False)
@@ -206,21 +235,59 @@ class OraclePagedKV:
 
         Returns ``(indices, indptr, last_page_len, valid_lens)``: FlashInfer's
         plan arguments for one request ([KVC] "Kernel-Level Execution Flow")
-        plus the number of valid tokens of every visible page.
-        """
+        plus the number of valid tokens of every visible page.  With a
+        special-token policy other than the default, see
+        ``visible_ranges`` (the pages' tokens then need not start at row 0)."""
+        indices, first_rows, valid = self.visible_ranges(block)
+        if not indices:
+            return [], [0, 0], 0, []
+        return indices, [0, len(indices)], valid[-1], valid
+
+    def visible_ranges(self, block=0):
+        """``(indices, first_rows, valid_lens)``: page i of the visible
+        sequence contributes its rows ``[first_rows[i], first_rows[i] +
+        valid_lens[i])``.  Order: scale pages, live window, special pages,
+        camera pages.
+
+        Default policy: every special page from row 0, the last one holding
+        ``last_page_len`` tokens ([KVC] "Physical Page Layout and Indexing":
+        compute_last_page_len).  The special stream position of a frame is its
+        append order, so the scale frames are positions ``[0, n_scale)`` and
+        the live frames ``[s - n_live, s)`` (appends go to the right end of the
+        live window, eviction takes its left end, rollback its right end).
+        Without cross-frame specials only those two runs are visible; with
+        camera_only the evicted frames' camera tokens, camera positions
+        ``[n_scale, s - n_live)``, are visible as well."""
         st = self._block(block)
         fpp = self.frames_per_special_page
         s = st.special_frames
-        n_sp = -(-s // fpp)
-        indices = list(st.scale) + list(st.live) + [self.num_patch_pages + i for i in range(n_sp)]
-        if not indices:
-            return [], [0, 0], 0, []
-        # Tokens in the last special page ([KVC] "Physical Page Layout and
-        # Indexing": compute_last_page_len).
-        last_page_len = NUM_SPECIAL * (s - fpp * (n_sp - 1))
-        valid = [self.page_size] * (len(st.scale) + len(st.live))
-        valid += [NUM_SPECIAL * fpp] * (n_sp - 1) + [last_page_len]
-        return indices, [0, len(indices)], last_page_len, valid
+        n_scale, n_live = len(st.scale), len(st.live)
+        indices = list(st.scale) + list(st.live)
+        first = [0] * len(indices)
+        valid = [self.page_size] * len(indices)
+        if self.cross_frame_special and not self.camera_only:
+            runs = [(0, s)]
+        elif n_scale >= s - n_live:
+            runs = [(0, s)]                      # nothing evicted yet
+        else:
+            runs = [(0, n_scale), (s - n_live, s)]
+        for a, b in runs:
+            # frames [a, b): page P + f // fpp, rows 6 (f % fpp) .. +6
+            for p in range(a // fpp, -(-b // fpp)) if b > a else ():
+                lo = max(a, p * fpp) - p * fpp
+                hi = min(b, (p + 1) * fpp) - p * fpp
+                indices.append(self.num_patch_pages + p)
+                first.append(NUM_SPECIAL * lo)
+                valid.append(NUM_SPECIAL * (hi - lo))
+        if self.camera_stream and n_scale < s - n_live:
+            a, b, ps = n_scale, s - n_live, self.page_size
+            for c in range(a // ps, -(-b // ps)):
+                lo = max(a, c * ps) - c * ps
+                hi = min(b, (c + 1) * ps) - c * ps
+                indices.append(self.first_camera_page + c)
+                first.append(lo)
+                valid.append(hi - lo)
+        return indices, first, valid
 
     def stats(self, block):
         """``get_cache_stats``: the five-field snapshot of [SLOTS] "动手验证"."""
@@ -244,10 +311,10 @@ class OraclePagedKV:
         block: [PERF] "One-Time Planning Pattern")."""
         if block not in self.mirror:
             raise ValueError(f"block {block} is not mirrored")
-        indices, _, _, valid = self.visible_page_table(plan_block)
+        indices, first, valid = self.visible_ranges(plan_block)
         m = self.mirror[block]
-        ks = [m[p, 0, :n] for p, n in zip(indices, valid)]
-        vs = [m[p, 1, :n] for p, n in zip(indices, valid)]
+        ks = [m[p, 0, r:r + n] for p, r, n in zip(indices, first, valid)]
+        vs = [m[p, 1, r:r + n] for p, r, n in zip(indices, first, valid)]
         if not ks:
             shape = (0, self.num_heads, self.head_dim)
             return np.zeros(shape, m.dtype), np.zeros(shape, m.dtype)
@@ -258,6 +325,13 @@ class OraclePagedKV:
         if not 0 <= block < self.num_blocks:
             raise OracleError("INVALID_ARG", f"block {block}")
         return self.blocks[block]
+
+    def _check_special_args(self, cross_frame_special, camera_only):
+        # The options are the construction's; another value is rejected.
+        if cross_frame_special is not None and bool(cross_frame_special) != self.cross_frame_special:
+            raise OracleError("INVALID_ARG", "cross_frame_special")
+        if camera_only is not None and bool(camera_only) != self.camera_only:
+            raise OracleError("INVALID_ARG", "camera_only")
 
     def _check_scale_arg(self, scale_frames, sliding_window):
         # Routing uses the constructor's scale_frames; a different value is rejected.

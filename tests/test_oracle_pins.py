@@ -134,6 +134,69 @@ def test_tiny_page_tables_match_hand_derivation():
     assert _check_hand_tables(OraclePagedKV) == []
 
 
+# Special-token policies (the reading of the eviction options cross_frame_special
+# and camera_only, [KVC] "Streaming Forward Pass"), same tiny stream.  The
+# frames of the scale pages are 0 and 1, the live window holds the newest
+# four; the special stream position of a frame is its append order, 2 frames
+# per special page (frame f: page 8 + f // 2, rows 6 (f % 2) .. +6).  With
+# camera_only one camera page follows the 8 special pages: page 16, camera
+# position f = row f.  Worked by hand:
+#   after 5 frames: nothing evicted yet (frames 0-1 scale, 2-4 live): every
+#     special of frames 0-4 -- pages 8, 9 (rows 0-11) and 10 (rows 0-5).
+#   after 7 frames: frame 2 evicted.  Scale specials: page 8 rows 0-11; live
+#     frames 3-6: frame 3 = page 9 rows 6-11, frames 4-5 = page 10 rows 0-11,
+#     frame 6 = page 11 rows 0-5.  camera_only adds camera page 16 row 2.
+#   after 12 frames: frames 2-7 evicted.  Scale: page 8 rows 0-11; live frames
+#     8-11: pages 12 and 13 rows 0-11.  camera_only adds page 16 rows 2-7.
+POLICY_TABLES = {
+    5: ([(8, 0, 12), (9, 0, 12), (10, 0, 6)], []),
+    7: ([(8, 0, 12), (9, 6, 6), (10, 0, 12), (11, 0, 6)], [(16, 2, 1)]),
+    12: ([(8, 0, 12), (12, 0, 12), (13, 0, 12)], [(16, 2, 6)]),
+}
+
+
+def _check_policy_tables(cache_cls):
+    bad = []
+    for cross, cam in ((False, False), (True, True), (False, True)):
+        c = cache_cls(num_blocks=1, page_size=16, num_heads=2, head_dim=32, dtype="f32",
+                      scale_frames=2, sliding_window=4, headroom=2, max_total_frames=16,
+                      mirror_blocks=(), cross_frame_special=cross, camera_only=cam)
+        for n in range(1, 13):
+            _stream(c, 0, 1)
+            if n not in POLICY_TABLES:
+                continue
+            idx, first, valid = c.visible_ranges(0)
+            scale, live, _ = c.deques(0)
+            special, camera = POLICY_TABLES[n]
+            want = [(p, 0, 16) for p in scale + live] + special + (camera if (cross and cam) else [])
+            if list(zip(idx, first, valid)) != want:
+                bad.append((cross, cam, n, list(zip(idx, first, valid))))
+    return bad
+
+
+def test_special_policy_tables_match_hand_derivation():
+    assert _check_policy_tables(OraclePagedKV) == []
+    # The default policy is the pages' two-stream table: every special page from row 0.
+    c = _tiny(mirror_blocks=())
+    _stream(c, 0, 12)
+    idx, first, valid = c.visible_ranges(0)
+    assert first == [0] * len(idx) and idx == HAND_TABLES[12][0]
+
+
+def test_special_policy_arguments_must_match_the_construction():
+    c = _tiny(mirror_blocks=(), cross_frame_special=False)
+    _stream(c, 0, 1)
+    c.evict_frames(0, 2, 4, cross_frame_special=False, camera_only=False)
+    for kw in ({"cross_frame_special": True}, {"camera_only": True}):
+        with pytest.raises(OracleError) as e:
+            c.evict_frames(0, 2, 4, **kw)
+        assert e.value.code == "INVALID_ARG"
+    # camera pages exist only with cross-frame specials kept camera-only
+    assert _tiny(camera_only=True).max_num_pages == 8 + 8 + 1
+    assert _tiny(camera_only=True, cross_frame_special=False).max_num_pages == 16
+    assert _tiny().max_num_pages == 16
+
+
 def test_full_size_end_states():
     # 518x378: 2048 frames, 166 frames per special page -> 13 special pages 88..100,
     # last page holds 2048 - 12*166 = 56 frames = 336 tokens.
@@ -274,14 +337,18 @@ def _sdpa64(q, k, v):
     return o[0].permute(1, 0, 2).numpy()
 
 
-def _check_transparency(cache_cls, mode="stream", seed=3, n=12):
+def _check_transparency(cache_cls, mode="stream", seed=3, n=12, cross=True, cam=False):
     """Attention over the paged cache vs attention over the frame-level
     visible set: patch tokens of the scale frames, of the live frames, then the
     special tokens of every kept frame in order ([SLOTS] '双流分页布局': visible
-    range = scale pages + window pages + all special pages)."""
+    range = scale pages + window pages + all special pages).  With the
+    special-token policies: without cross-frame specials only the scale and
+    live frames' specials; with camera_only those plus the camera token (row
+    0) of every other kept frame."""
     rng = np.random.default_rng(seed)
     c = cache_cls(num_blocks=1, page_size=16, num_heads=2, head_dim=32, dtype="f32",
-                  scale_frames=2, sliding_window=4, headroom=3, max_total_frames=16)
+                  scale_frames=2, sliding_window=4, headroom=3, max_total_frames=16,
+                  cross_frame_special=cross, camera_only=cam)
     kept = []                                   # (k, v) of committed or pending frames
     worst = 0.0
     for f in range(n):
@@ -301,8 +368,16 @@ def _check_transparency(cache_cls, mode="stream", seed=3, n=12):
         else:
             n_live = min(4, max(0, len(kept) - 2))
         live_fr = kept[len(kept) - n_live:] if n_live > 0 else []
-        K = np.concatenate([x[6:] for x, _ in scale_fr + live_fr] + [x[:6] for x, _ in kept])
-        V = np.concatenate([y[6:] for _, y in scale_fr + live_fr] + [y[:6] for _, y in kept])
+        evicted = kept[2:len(kept) - n_live]
+        if cross and not cam:
+            spec = [x[:6] for x, _ in kept], [y[:6] for _, y in kept]
+        else:
+            window = scale_fr + live_fr
+            spec = [x[:6] for x, _ in window], [y[:6] for _, y in window]
+            if cross and cam:
+                spec = spec[0] + [x[:1] for x, _ in evicted], spec[1] + [y[:1] for _, y in evicted]
+        K = np.concatenate([x[6:] for x, _ in scale_fr + live_fr] + spec[0])
+        V = np.concatenate([y[6:] for _, y in scale_fr + live_fr] + spec[1])
         want = _sdpa64(qf.astype(np.float64), K.astype(np.float64), V.astype(np.float64))
         got = paged_attention(c, 0, qb)
         worst = max(worst, float(np.abs(got - want).max()))
@@ -321,6 +396,12 @@ def test_paging_is_transparent_stream():
 
 def test_paging_is_transparent_defer():
     assert _check_transparency(OraclePagedKV, "defer", seed=5, n=16) < 1e-12
+
+
+@pytest.mark.parametrize("cross,cam", [(False, False), (True, True), (False, True)])
+@pytest.mark.parametrize("mode", ["stream", "defer"])
+def test_paging_is_transparent_special_policies(cross, cam, mode):
+    assert _check_transparency(OraclePagedKV, mode, seed=7, n=16, cross=cross, cam=cam) < 1e-12
 
 
 def test_cache_bytes_are_the_frame_rows():
@@ -453,12 +534,12 @@ class _EvictToFront(OraclePagedKV):
 class _FullSpecialPages(OraclePagedKV):
     """Planted mistake: every non-last special page counted as full (page_size)."""
 
-    def visible_page_table(self, block=0):
-        idx, indptr, lpl, valid = super().visible_page_table(block)
+    def visible_ranges(self, block=0):
+        idx, first, valid = super().visible_ranges(block)
         n_patch = len(self.blocks[block].scale) + len(self.blocks[block].live)
         valid = [self.page_size if (i >= n_patch and i < len(valid) - 1) else n
                  for i, n in enumerate(valid)]
-        return idx, indptr, lpl, valid
+        return idx, first, valid
 
 
 class _LiveBeforeScale(OraclePagedKV):
@@ -471,7 +552,36 @@ class _LiveBeforeScale(OraclePagedKV):
         return idx[ns:ns + nl] + idx[:ns] + idx[ns + nl:], indptr, lpl, valid
 
 
+class _CameraRunOffByOne(OraclePagedKV):
+    """Planted mistake: the evicted frames' camera run starts one frame late."""
+
+    def visible_ranges(self, block=0):
+        idx, first, valid = super().visible_ranges(block)
+        if self.camera_stream and idx and idx[-1] >= self.first_camera_page and valid[-1] > 1:
+            first[-1] += 1
+            valid[-1] -= 1
+        return idx, first, valid
+
+
+class _EvictedSpecialsKept(OraclePagedKV):
+    """Planted mistake: without cross-frame specials, the evicted frames'
+    specials are still attended (the default table)."""
+
+    def visible_ranges(self, block=0):
+        if not self.cross_frame_special:
+            self.cross_frame_special = True
+            try:
+                return super().visible_ranges(block)
+            finally:
+                self.cross_frame_special = False
+        return super().visible_ranges(block)
+
+
 def test_planted_mistakes_are_caught():
+    assert _check_policy_tables(_CameraRunOffByOne) != []
+    assert _check_policy_tables(_EvictedSpecialsKept) != []
+    assert _check_transparency(_CameraRunOffByOne, seed=7, n=16, cam=True) > 1e-6
+    assert _check_transparency(_EvictedSpecialsKept, seed=7, n=16, cross=False) > 1e-6
     assert _check_hand_tables(_EvictToFront) != []
     assert _check_hand_tables(_LiveBeforeScale) != []
     assert _check_transparency(_FullSpecialPages) > 1e-6
