@@ -14,9 +14,14 @@
 // Host code must not hand the array's name to a kernel: in host code that
 // name is a host-side stand-in, not a device address.  The device address is
 // taken once per device with cudaGetSymbolAddress while that device is
-// current (setup_device below) and passed to the kernels.
+// current (setup_device below) and passed to the kernels.  It is remembered
+// together with the context it was taken in: if that context is destroyed and
+// a new one made (cudaDeviceReset), the module is loaded again, possibly at
+// another address, and the next call looks the address up again.
 #include "kvc.h"
 #include "kvc_internal.h"
+
+#include <cuda.h>
 
 #include <algorithm>
 #include <cmath>
@@ -39,19 +44,44 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char* g_scratch_dev[kMaxDevices];   // device address per device, once set up
+CUcontext g_scratch_ctx[kMaxDevices];        // the context that address belongs to
 int g_num_sms[kMaxDevices];
 
-// Once per device, with that device current: the array's device address and
-// the SM count.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The driver's current context, through the runtime's entry-point query (no
+// link against the driver library).
+bool current_context(CUcontext* ctx) {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  *ctx = nullptr;
+  return fn && fn(ctx) == CUDA_SUCCESS && *ctx != nullptr;
+}
+
+// Once per device (and again if its context was replaced), with that device
+// current: the array's device address and the SM count.
 int setup_device(int dev) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_dev[dev]) return KVC_OK;
+  // Before the runtime's first call on this thread there may be no current
+  // context yet; the symbol lookup below makes the device's context current.
+  CUcontext ctx = nullptr;
+  if (current_context(&ctx) && g_scratch_dev[dev] && g_scratch_ctx[dev] == ctx) return KVC_OK;
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return KVC_ERR_CUDA;
+  if (!current_context(&ctx)) return KVC_ERR_CUDA;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVC_ERR_CUDA;
   g_num_sms[dev] = sms;
   g_scratch_dev[dev] = static_cast<unsigned char*>(p);
+  g_scratch_ctx[dev] = ctx;
   return KVC_OK;
 }
 
@@ -167,6 +197,7 @@ extern "C" int kvc_paged_attention_static(const void* cache_block, int32_t dtype
   a.page_size = page_size;
   a.n_tiles = (int32_t)n_tiles;
   a.n_splits = splits;
+  a.max_pages = 0x7fffffff;   // the caller's cache extent is not known here
   const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt((float)head_dim);
   a.sm_scale_log2 = scale * 1.4426950408889634f;
   a.wait_budget = 4000000000LL;
