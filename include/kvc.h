@@ -59,7 +59,8 @@ enum {
   KVC_ERR_DEVICE_TIMEOUT = -9,      /* a kernel gave up waiting (kvc_device_status)  */
   KVC_ERR_EMPTY = -10,              /* plan of a cache with no visible token         */
   KVC_ERR_NO_DEVICE = -11,          /* device call on a bookkeeping-only handle      */
-  KVC_ERR_TOO_LARGE = -12           /* beyond kvc_paged_attention_static's scratch   */
+  KVC_ERR_TOO_LARGE = -12,          /* beyond kvc_paged_attention_static's scratch   */
+  KVC_ERR_DEVICE_BOUNDS = -13       /* a bounds check failed (KVC_CHECKED builds)    */
 };
 
 typedef struct kvc_handle kvc_handle;
@@ -85,7 +86,27 @@ typedef struct {
   float sm_scale;             /* softmax scale; 0 => 1/sqrt(head_dim)              */
   int32_t max_query_tokens;   /* largest n_q of kvc_run; 0 => 6 + page_size        */
   int32_t max_kv_splits;      /* split-KV partial buffers; 0 => 32                 */
+  int32_t special_policy;     /* KVC_SPECIAL_* flags; 0 => every frame's specials  */
 } kvc_config;
+
+/* What stays visible of an evicted frame's special tokens: the eviction
+ * options cross_frame_special and camera_only that the block passes to
+ * evict_frames ([KVC] "Streaming Forward Pass").  The pages do not say what
+ * they do; this library reads them as follows.
+ *   0 (cross_frame_special on, camera_only off): every frame's six specials
+ *     stay visible after its patch page is evicted -- the pages' two-stream
+ *     behaviour ([SLOTS] "特殊 token 流": the special stream is never evicted).
+ *   KVC_SPECIAL_NO_CROSS_FRAME (cross_frame_special off): a frame's specials
+ *     leave the visible set together with its patch page; the scale and live
+ *     frames' specials stay.  camera_only then changes nothing.
+ *   KVC_SPECIAL_CAMERA_ONLY (camera_only on): of an evicted frame's specials
+ *     only the camera token (the first of the six) stays visible.  Every
+ *     frame's camera token is then also written to a third append-only
+ *     stream, the camera pages (page_size tokens per page, after the special
+ *     pages; see kvc_get_geometry), so that the evicted frames' camera
+ *     tokens form one contiguous run.
+ * The special stream itself is the same in every policy. */
+enum { KVC_SPECIAL_NO_CROSS_FRAME = 1, KVC_SPECIAL_CAMERA_ONLY = 2 };
 
 /* get_cache_stats snapshot ([SLOTS] "动手验证"). */
 typedef struct {
@@ -99,6 +120,24 @@ typedef struct {
 /* Byte sizes of the cache and of the workspace (plan tables, split-KV partial
  * outputs and the device status word) for `cfg`.  Validates cfg. */
 int kvc_required_bytes(const kvc_config* cfg, size_t* cache_bytes, size_t* workspace_bytes);
+
+/* Page geometry of the cache `cfg` describes ([PERF] "Two-Stream Page Pool
+ * Architecture"; [SLOTS] "双流分页布局", "特殊 token 流"): P =
+ * scale_frames + sliding_window + headroom patch pages, floor(page_size / 6)
+ * frames per special page, ceil(max_total_frames / that) special pages; one
+ * block's cache is [max_num_pages][2][page_size][H][D] (page_bytes per page,
+ * block_bytes per block, blocks back to back).  Validates cfg. */
+typedef struct {
+  int32_t num_patch_pages;
+  int32_t frames_per_special_page;
+  int32_t num_special_pages;
+  int32_t num_camera_pages;   /* KVC_SPECIAL_CAMERA_ONLY: ceil(max_total_frames / page_size), else 0 */
+  int32_t max_num_pages;      /* patch + special + camera pages */
+  int32_t tokens_per_frame;   /* 6 + page_size */
+  int64_t page_bytes;
+  int64_t block_bytes;
+} kvc_geometry;
+int kvc_get_geometry(const kvc_config* cfg, kvc_geometry* out);
 
 /* Create a handle.  cache_dev / workspace_dev: caller-owned device buffers of
  * the sizes above, 256-byte aligned; the cache is zero-filled and the
@@ -131,6 +170,13 @@ int kvc_append_frame(kvc_handle* h, int32_t block, const void* K, const void* V,
  * while eviction is deferred.  An eviction that moves a page commits the
  * block's pending frames.  scale_frames must equal the configured value. */
 int kvc_evict_frames(kvc_handle* h, int32_t block, int32_t scale_frames, int32_t sliding_window);
+
+/* evict_frames with the block's two eviction options as the pages pass them
+ * ([KVC] "Streaming Forward Pass": cross_frame_special, camera_only; nonzero =
+ * on).  They must match the cache's special_policy (as scale_frames must
+ * match the configured value), else INVALID_ARG; then as kvc_evict_frames. */
+int kvc_evict_frames_ex(kvc_handle* h, int32_t block, int32_t scale_frames, int32_t sliding_window,
+                        int32_t cross_frame_special, int32_t camera_only);
 
 /* Manager-wide deferral switch, the `_defer_eviction` attribute ([PERF]
  * "Deferred Eviction Strategy"). */
@@ -212,6 +258,14 @@ int kvc_get_cache_stats(const kvc_handle* h, int32_t block, kvc_stats* out);
 int kvc_get_plan(const kvc_handle* h, int32_t* indptr2, int32_t* indices, int32_t cap,
                  int32_t* n_pages, int32_t* last_page_len);
 
+/* Host copy of the current plan as row ranges: visible entry i is rows
+ * [first_rows[i], first_rows[i] + valid_lens[i]) of page indices[i] (with the
+ * default special policy every first row is 0 and this is kvc_get_plan's
+ * table).  Arrays of cap entries, any may be NULL.  Errors: NO_PLAN,
+ * INVALID_ARG (cap too small; n_pages is still written). */
+int kvc_get_plan_ranges(const kvc_handle* h, int32_t* indices, int32_t* first_rows, int32_t* valid_lens,
+                        int32_t cap, int32_t* n_pages);
+
 /* Snapshot of a block's deques (left to right) for parity checks; each array
  * needs room for P entries.  Any pointer may be NULL. */
 int kvc_get_deques(const kvc_handle* h, int32_t block, int32_t* scale, int32_t* n_scale,
@@ -223,7 +277,15 @@ int kvc_get_deques(const kvc_handle* h, int32_t block, int32_t* scale, int32_t* 
 int kvc_read_device_plan(kvc_handle* h, int32_t* indices, int32_t* valid_lens, int32_t cap,
                          int32_t* n_pages, int32_t* last_page_len, kvc_stream stream);
 
+/* The device page table as row ranges (indices, first rows, valid counts);
+ * for parity tests; synchronises `stream`. */
+int kvc_read_device_ranges(kvc_handle* h, int32_t* indices, int32_t* first_rows, int32_t* valid_lens,
+                           int32_t cap, int32_t* n_pages, kvc_stream stream);
+
 /* Read and clear the device status word (synchronises `stream`).  Returns
+ * KVC_ERR_DEVICE_BOUNDS if a kernel of a KVC_CHECKED build found a page id,
+ * slot, tile row or TMA coordinate outside the cache (it skipped the access);
+ * else
  * KVC_OK, or KVC_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait
  * since the last call. */
 int kvc_device_status(kvc_handle* h, kvc_stream stream);
@@ -234,9 +296,12 @@ enum {
   KVC_OPT_NUM_SPLITS = 2,  /* 0 auto, else the number of KV splits (<= max_kv_splits)     */
   KVC_OPT_WAIT_BUDGET = 3, /* bounded-wait budget in SM clock cycles; 0 => default (~2 s) */
   KVC_OPT_TIMING = 4,      /* 1: time every attention launch with CUDA events            */
-  KVC_OPT_STALL_TEST = 5   /* test only, 1: the tensor-core kernel first waits on a barrier
+  KVC_OPT_STALL_TEST = 5,  /* test only, 1: the tensor-core kernel first waits on a barrier
                               that nothing signals, so its bounded wait runs out and the run
                               reports KVC_ERR_DEVICE_TIMEOUT (no output is written)           */
+  KVC_OPT_QUERY_TILES = 6  /* tensor-core kernel: 128-row query tiles per CTA; 0 auto,
+                              1 (both softmax warp groups share one tile, taking alternate
+                              KV tiles), 2 (one warp group per tile)                         */
 };
 int kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
 
@@ -264,7 +329,10 @@ int kvc_get_counters(kvc_handle* h, int64_t* kernel_launches, int64_t* attn_laun
  * head_dim 128), else KVC_ERR_TOO_LARGE; the number of KV splits is cut to
  * what fits in the array.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  Every call shares the one array, so
+ * first call before any stream capture.  The address is kept with the CUDA
+ * context it belongs to: after cudaDeviceReset (or any other replacement of
+ * the device's context) the next call looks it up again, so it too must come
+ * before any capture.  Every call shares the one array, so
  * calls whose work overlaps on the GPU (other streams, other threads) race:
  * serialise them.  The status word is cleared on every call. */
 int kvc_paged_attention_static(const void* cache_block, int32_t dtype, int32_t num_heads,

@@ -20,6 +20,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkvc.so")
 STAMP = os.path.join(PKG, "libkvc.machine")
+# KVC_CHECKED=1: the same library with device-side bounds checks, built beside it.
+LIB_CHECKED = os.path.join(PKG, "libkvc_checked.so")
+STAMP_CHECKED = os.path.join(PKG, "libkvc_checked.machine")
 SOURCES = ["kvc_host.cpp", "kvc_kernels.cu", "kvc_attn_tc.cu", "kvc_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -33,21 +36,27 @@ def nvcc():
     raise RuntimeError("nvcc not found")
 
 
-def _stale():
-    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+def _stale(lib=LIB, stamp=STAMP):
+    if not os.path.exists(lib) or not os.path.exists(stamp):
         return True
-    if open(STAMP).read().strip() != platform.machine():
+    if open(stamp).read().strip() != platform.machine():
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "kvc.h"), __file__]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force=False, verbose=False, extra_flags=()):
-    """Compile and link libkvc.so; returns its path."""
-    if not force and not _stale():
-        return LIB
-    out_dir = os.path.join(PKG, "_build", platform.machine())
+def build(force=False, verbose=False, extra_flags=(), checked=None):
+    """Compile and link libkvc.so (with checked=True, or KVC_CHECKED=1 in the
+    environment: libkvc_checked.so, with -DKVC_CHECKED=1); returns its path."""
+    if checked is None:
+        checked = os.environ.get("KVC_CHECKED") == "1"
+    lib, stamp = (LIB_CHECKED, STAMP_CHECKED) if checked else (LIB, STAMP)
+    if checked:
+        extra_flags = tuple(extra_flags) + ("-DKVC_CHECKED=1",)
+    if not force and not _stale(lib, stamp):
+        return lib
+    out_dir = os.path.join(PKG, "_build", platform.machine() + ("-checked" if checked else ""))
     os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
 
@@ -65,15 +74,15 @@ def build(force=False, verbose=False, extra_flags=()):
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
         f.write(platform.machine() + "\n")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

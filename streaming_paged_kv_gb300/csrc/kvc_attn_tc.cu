@@ -146,6 +146,13 @@ __device__ __noinline__ void raise_abort(const Guard& g, int where) {
   __threadfence();
 }
 
+// Checked builds: a tile outside its cache records the failure (code, where,
+// value) and aborts the CTA through the same path as a timed-out wait.
+__device__ __noinline__ void raise_bounds(const Guard& g, int where, int value) {
+  *g.abort_flag = 1;
+  record_bounds(g.status, where, value);
+}
+
 __device__ __forceinline__ bool wait_bar(const Guard& g, uint64_t* bar, uint32_t parity, int where) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
@@ -385,7 +392,7 @@ struct TcRequest {
   float* part_o;           // [n_splits][n_q][H][D] (n_splits > 1)
   float* part_lse;         // [n_splits][n_q][H]
   int32_t* status;
-  int32_t n_tiles, n_splits, q_row0, n_q, page_base, cta0, q_blocks, pad;
+  int32_t n_tiles, n_splits, q_row0, n_q, page_base, cta0, q_blocks, max_pages, page_size;
 };
 struct TcLaunch {
   CUtensorMap q_map;       // [rows, H * D] over every request's query rows
@@ -393,6 +400,7 @@ struct TcLaunch {
   void* out;               // [rows, H, D]
   int32_t count, num_heads, stall_test;
   int32_t allow_dual;      // single-query-tile CTAs may use dual mode (three or more waves of CTAs)
+  int32_t q_rows_cta;      // query rows per CTA: 256 (two tiles) or 128 (one tile)
   float sm_scale_log2;
   long long wait_budget;
   TcRequest req[kTcMaxBatch];
@@ -438,8 +446,8 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
   const int qblock = local % R.q_blocks;
   const int h = (local / R.q_blocks) % P.num_heads;
   const int split = local / (R.q_blocks * P.num_heads);
-  const int q0 = qblock * (QT * BM);              // first query row within the request
-  const bool has_q1 = q0 + BM < R.n_q;
+  const int q0 = qblock * P.q_rows_cta;           // first query row within the request
+  const bool has_q1 = P.q_rows_cta > BM && q0 + BM < R.n_q;
   const int nq = has_q1 ? 2 : 1;
   const int t0 = (int)(((int64_t)split * R.n_tiles) / R.n_splits);
   const int t1 = (int)(((int64_t)(split + 1) * R.n_tiles) / R.n_splits);
@@ -502,6 +510,12 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
         if (j >= STAGES && !wait_bar_warp(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
         const KvTile tile = tiles[t0 + j];
         const int plane = (R.page_base + tile.page) * 2;
+        if (KVC_CHECKED && (tile.page < 0 || tile.page >= R.max_pages || tile.row0 < 0 || tile.rows < 1 ||
+                            tile.rows > BN || tile.row0 + tile.rows > R.page_size || h >= P.num_heads)) {
+          if (leader) raise_bounds(g, 401, t0 + j);
+          __syncwarp();
+          break;
+        }
         if (leader) {
           mbar_expect_tx(&kv_full[st], 2 * TILE_BYTES);
           tma_load_3d(sK + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane, &kv_full[st]);
@@ -896,6 +910,7 @@ void tc_destroy_maps(TcMaps* m) { delete m; }
 cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || b.count < 1 || b.count > kTcMaxBatch || b.head_dim != HD) return cudaErrorNotSupported;
+  if (b.q_tiles != 1 && b.q_tiles != QT) return cudaErrorInvalidValue;
   TcLaunch P;
   std::memset(&P, 0, sizeof(P));
   const cuuint64_t row_bytes = (cuuint64_t)b.num_heads * HD * 2;
@@ -913,6 +928,7 @@ cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
   P.stall_test = b.stall_test;
   P.sm_scale_log2 = b.sm_scale_log2;
   P.wait_budget = b.wait_budget;
+  P.q_rows_cta = b.q_tiles * BM;
   int64_t ctas = 0;
   for (int r = 0; r < b.count; ++r) {
     const TcRequestDesc& d = b.req[r];
@@ -929,12 +945,16 @@ cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
     q.q_row0 = d.q_row0;
     q.n_q = d.n_q;
     q.page_base = d.block * d.max_pages;
-    q.q_blocks = (d.n_q + QT * BM - 1) / (QT * BM);
+    q.max_pages = d.max_pages;
+    q.page_size = d.page_size;
+    q.q_blocks = (d.n_q + P.q_rows_cta - 1) / P.q_rows_cta;
     q.cta0 = (int32_t)ctas;
     ctas += (int64_t)q.q_blocks * b.num_heads * d.n_splits;
   }
   if (ctas == 0) return cudaSuccess;
-  P.allow_dual = ctas > 2 * (int64_t)b.num_sms ? 1 : 0;   // measured: helps from about three waves on
+  // Two-tile CTAs: dual mode for their single-tile tail only from about three
+  // waves on (measured).  One-tile CTAs always run in dual mode.
+  P.allow_dual = (b.q_tiles == 1 || ctas > 2 * (int64_t)b.num_sms) ? 1 : 0;
   if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
   const int which = b.dtype == 0 ? 0 : 1;
   auto kernel = which == 0 ? attn_tc_kernel<true> : attn_tc_kernel<false>;

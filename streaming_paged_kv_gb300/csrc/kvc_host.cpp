@@ -17,6 +17,7 @@
 #include "kvc_internal.h"
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdlib>
@@ -91,14 +92,20 @@ int resolve(const kvc_config* in, kvc_config* out) {
   if (c.max_kv_splits < 1 || c.max_kv_splits > 256) return KVC_ERR_INVALID_ARG;
   if (!(c.sm_scale > 0.0f) || !std::isfinite(c.sm_scale)) return KVC_ERR_INVALID_ARG;
   if (((int64_t)c.num_heads * c.head_dim * elem_bytes(c.dtype)) % 16 != 0) return KVC_ERR_INVALID_ARG;
+  if (c.special_policy < 0 || c.special_policy > (KVC_SPECIAL_NO_CROSS_FRAME | KVC_SPECIAL_CAMERA_ONLY))
+    return KVC_ERR_INVALID_ARG;
   *out = c;
   return KVC_OK;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Evicted frames keep only their camera token visible (needs the camera stream).
+bool camera_stream(const kvc_config& c) { return c.special_policy == KVC_SPECIAL_CAMERA_ONLY; }
+bool cross_frame(const kvc_config& c) { return (c.special_policy & KVC_SPECIAL_NO_CROSS_FRAME) == 0; }
+
 struct Geometry {
-  int32_t P, fpp, n_special_pages, max_pages, T;
+  int32_t P, fpp, n_special_pages, n_camera_pages, first_camera, max_pages, max_entries, T;
   int64_t row_bytes, page_bytes, block_bytes;
   size_t cache_bytes;
   kvc::WorkspaceLayout L;
@@ -108,7 +115,13 @@ void geometry(const kvc_config& c, Geometry* g) {
   g->P = c.scale_frames + c.sliding_window + c.headroom;
   g->fpp = c.page_size / kNumSpecial;                      // floor(page_size / 6)
   g->n_special_pages = (c.max_total_frames + g->fpp - 1) / g->fpp;
-  g->max_pages = g->P + g->n_special_pages;
+  // Camera stream: page_size camera tokens per page, after the special pages.
+  g->n_camera_pages = camera_stream(c) ? (c.max_total_frames + c.page_size - 1) / c.page_size : 0;
+  g->first_camera = g->P + g->n_special_pages;
+  g->max_pages = g->P + g->n_special_pages + g->n_camera_pages;
+  // Visible entries: every page at most once, except that the two special
+  // runs of a policy without cross-frame specials may share a page each end.
+  g->max_entries = g->max_pages + 2;
   g->T = kNumSpecial + c.page_size;
   g->row_bytes = (int64_t)c.num_heads * c.head_dim * elem_bytes(c.dtype);
   g->page_bytes = 2 * (int64_t)c.page_size * g->row_bytes;  // K and V of one page
@@ -116,20 +129,21 @@ void geometry(const kvc_config& c, Geometry* g) {
   g->cache_bytes = (size_t)g->block_bytes * c.num_blocks;
   // The smallest tile any attention kernel uses bounds the tile count.
   const int min_rows = 32;
-  int64_t max_tiles = (int64_t)g->max_pages * ((c.page_size + min_rows - 1) / min_rows);
+  int64_t max_tiles = (int64_t)g->max_entries * ((c.page_size + min_rows - 1) / min_rows);
   kvc::WorkspaceLayout& L = g->L;
   size_t off = 0;
   L.status = off;   off += 256;
   L.header = off;   off += 256;
-  L.page_ids = off; off = align_up(off + 4 * (size_t)g->max_pages, 256);
-  L.page_valid = off; off = align_up(off + 4 * (size_t)g->max_pages, 256);
+  L.page_ids = off; off = align_up(off + 4 * (size_t)g->max_entries, 256);
+  L.page_valid = off; off = align_up(off + 4 * (size_t)g->max_entries, 256);
+  L.page_row0 = off; off = align_up(off + 4 * (size_t)g->max_entries, 256);
   L.tiles = off;    off = align_up(off + sizeof(kvc::KvTile) * (size_t)max_tiles, 256);
   L.part_o = off;
   off = align_up(off + 4 * (size_t)c.max_kv_splits * c.max_query_tokens * c.num_heads * c.head_dim, 256);
   L.part_lse = off;
   off = align_up(off + 4 * (size_t)c.max_kv_splits * c.max_query_tokens * c.num_heads, 256);
   L.total = off;
-  L.max_pages = g->max_pages;
+  L.max_pages = g->max_entries;
   L.max_tiles = (int32_t)max_tiles;
 }
 
@@ -150,12 +164,15 @@ struct kvc_handle {
   bool has_plan = false;
   int32_t plan_n_pages = 0, plan_lpl = 0, plan_n_tiles = 0, plan_tile_rows = 0, plan_kernel = 0;
   int32_t plan_n_scale = 0, plan_n_live = 0, plan_special_frames = 0;
-  int32_t* plan_ids = nullptr;      // [max_pages]
+  int32_t* plan_ids = nullptr;      // [max_entries]
+  int32_t* plan_row0 = nullptr;     // [max_entries]
+  int32_t* plan_valid = nullptr;    // [max_entries]
   int32_t* plan_snapshot = nullptr; // [P]: scale then live
   kvc::PlanArgs* plan_args = nullptr;
   // Options.
   int opt_kernel = 0;
   int opt_splits = 0;
+  int opt_qtiles = 0;
   long long wait_budget = 0;
   bool timing = false;
   int stall_test = 0;
@@ -169,6 +186,13 @@ struct kvc_handle {
 };
 
 namespace {
+
+// NVTX range over a call (header-only NVTX 3: costs nothing unless a
+// profiler is attached), so that timelines show append / plan / run.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 int check_block(const kvc_handle* h, int32_t block) {
   if (!h || block < 0 || block >= h->cfg.num_blocks) return KVC_ERR_INVALID_ARG;
@@ -197,6 +221,9 @@ int attn_kernel_for(const kvc_handle* h) {
   return tc ? 2 : 1;
 }
 
+// Query tiles (128 rows) per CTA of the tensor-core kernel.
+int q_tiles_for(const kvc_handle* h) { return h->opt_qtiles > 0 ? h->opt_qtiles : 2; }
+
 int tile_rows_for(const kvc_handle* h, int kernel) {
   return kernel == 2 ? kvc::kTcTileRows : kvc::simt_tile_rows(h->cfg.head_dim);
 }
@@ -208,7 +235,7 @@ int choose_splits(const kvc_handle* h, int kernel, int32_t n_q) {
   if (max_s > h->plan_n_tiles) max_s = h->plan_n_tiles;
   if (max_s < 1) max_s = 1;
   if (h->opt_splits > 0) return h->opt_splits < max_s ? h->opt_splits : max_s;
-  int q_rows = kernel == 2 ? kvc::kTcQRows : 128;
+  int q_rows = kernel == 2 ? 128 * q_tiles_for(h) : 128;
   int64_t base = (int64_t)((n_q + q_rows - 1) / q_rows) * h->cfg.num_heads;
   int64_t slots = (int64_t)h->num_sms * (kernel == 2 ? 1 : 2);
   double best = 1e300;
@@ -287,6 +314,7 @@ kvc::AttnArgs attn_args(const kvc_handle* h, int32_t block, const void* Q, void*
   a.page_size = h->cfg.page_size;
   a.n_tiles = h->plan_n_tiles;
   a.n_splits = splits;
+  a.max_pages = h->g.max_pages;
   a.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
   a.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
   a.stall_test = h->stall_test;
@@ -304,6 +332,7 @@ kvc::TcBatchArgs tc_batch_header(const kvc_handle* h, const void* Q, void* out, 
   tb.dtype = h->cfg.dtype;
   tb.stall_test = h->stall_test;
   tb.num_sms = h->num_sms;
+  tb.q_tiles = q_tiles_for(h);
   tb.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
   tb.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
   return tb;
@@ -314,6 +343,7 @@ kvc::TcRequestDesc tc_request(const kvc_handle* h, int32_t block, int32_t q_row0
   d.maps = h->maps;
   d.block = block;
   d.max_pages = h->g.max_pages;
+  d.page_size = h->cfg.page_size;
   d.tiles = (const kvc::KvTile*)(h->ws + h->g.L.tiles);
   d.part_o = (float*)(h->ws + h->g.L.part_o);
   d.part_lse = (float*)(h->ws + h->g.L.part_lse);
@@ -326,6 +356,24 @@ kvc::TcRequestDesc tc_request(const kvc_handle* h, int32_t block, int32_t q_row0
 }
 
 extern "C" {
+
+int kvc_get_geometry(const kvc_config* cfg, kvc_geometry* out) {
+  kvc_config c;
+  int rc = resolve(cfg, &c);
+  if (rc) return rc;
+  if (!out) return KVC_ERR_INVALID_ARG;
+  Geometry g;
+  geometry(c, &g);
+  out->num_patch_pages = g.P;
+  out->frames_per_special_page = g.fpp;
+  out->num_special_pages = g.n_special_pages;
+  out->num_camera_pages = g.n_camera_pages;
+  out->max_num_pages = g.max_pages;
+  out->tokens_per_frame = g.T;
+  out->page_bytes = g.page_bytes;
+  out->block_bytes = g.block_bytes;
+  return KVC_OK;
+}
 
 int kvc_required_bytes(const kvc_config* cfg, size_t* cache_bytes, size_t* workspace_bytes) {
   kvc_config c;
@@ -355,11 +403,13 @@ int kvc_create(const kvc_config* cfg, void* cache_dev, void* workspace_dev, kvc_
   h->blocks = new (std::nothrow) Block[c.num_blocks];
   h->ring_storage = (int32_t*)std::calloc((size_t)c.num_blocks * 3 * P, sizeof(int32_t));
   h->undo_storage = (Undo*)std::calloc((size_t)c.num_blocks * P, sizeof(Undo));
-  h->plan_ids = (int32_t*)std::calloc((size_t)h->g.max_pages, sizeof(int32_t));
+  h->plan_ids = (int32_t*)std::calloc((size_t)h->g.max_entries, sizeof(int32_t));
+  h->plan_row0 = (int32_t*)std::calloc((size_t)h->g.max_entries, sizeof(int32_t));
+  h->plan_valid = (int32_t*)std::calloc((size_t)h->g.max_entries, sizeof(int32_t));
   h->plan_snapshot = (int32_t*)std::calloc((size_t)P, sizeof(int32_t));
   h->plan_args = (kvc::PlanArgs*)std::calloc(1, sizeof(kvc::PlanArgs));
-  if (!h->blocks || !h->ring_storage || !h->undo_storage || !h->plan_ids || !h->plan_snapshot ||
-      !h->plan_args) {
+  if (!h->blocks || !h->ring_storage || !h->undo_storage || !h->plan_ids || !h->plan_row0 ||
+      !h->plan_valid || !h->plan_snapshot || !h->plan_args) {
     kvc_destroy(h);
     return KVC_ERR_INVALID_ARG;
   }
@@ -412,6 +462,8 @@ int kvc_destroy(kvc_handle* h) {
   std::free(h->ring_storage);
   std::free(h->undo_storage);
   std::free(h->plan_ids);
+  std::free(h->plan_row0);
+  std::free(h->plan_valid);
   std::free(h->plan_snapshot);
   std::free(h->plan_args);
   delete h;
@@ -419,6 +471,7 @@ int kvc_destroy(kvc_handle* h) {
 }
 
 int kvc_append_frame(kvc_handle* h, int32_t block, const void* K, const void* V, kvc_stream stream) {
+  NvtxRange range("kvc_append_frame");
   int rc = check_block(h, block);
   if (rc) return rc;
   if (h->device ? (!K || !V || !aligned16(K) || !aligned16(V)) : (K || V)) return KVC_ERR_INVALID_ARG;
@@ -430,10 +483,14 @@ int kvc_append_frame(kvc_handle* h, int32_t block, const void* K, const void* V,
   const int32_t s = b.special_frames;
   const int32_t sp_page = h->g.P + s / h->g.fpp;
   const int32_t sp_slot = kNumSpecial * (s % h->g.fpp);
+  // Camera stream: the camera token (row 0) also goes to camera position s.
+  const int32_t cam_page = camera_stream(h->cfg) ? h->g.first_camera + s / h->cfg.page_size : -1;
+  const int32_t cam_slot = s % h->cfg.page_size;
   if (h->device) {
     char* cache_block = h->cache + (size_t)block * h->g.block_bytes;
-    cudaError_t err = kvc::launch_append(cache_block, K, V, page, sp_page, sp_slot, h->cfg.page_size,
-                                         h->g.row_bytes, (cudaStream_t)stream);
+    cudaError_t err = kvc::launch_append(cache_block, K, V, page, sp_page, sp_slot, cam_page, cam_slot,
+                                         h->cfg.page_size, h->g.row_bytes, h->g.max_pages,
+                                         (int32_t*)(h->ws + h->g.L.status), (cudaStream_t)stream);
     if (err != cudaSuccess) return KVC_ERR_CUDA;
     ++h->launches;
   }
@@ -454,6 +511,17 @@ int kvc_evict_frames(kvc_handle* h, int32_t block, int32_t scale_frames, int32_t
   if (h->defer) return KVC_OK;
   evict_to(h->blocks[block], sliding_window, false);
   return KVC_OK;
+}
+
+int kvc_evict_frames_ex(kvc_handle* h, int32_t block, int32_t scale_frames, int32_t sliding_window,
+                        int32_t cross_frame_special, int32_t camera_only) {
+  int rc = check_block(h, block);
+  if (rc) return rc;
+  // The options are the cache's (kvc_config.special_policy), like scale_frames.
+  if ((cross_frame_special != 0) != cross_frame(h->cfg) ||
+      (camera_only != 0) != ((h->cfg.special_policy & KVC_SPECIAL_CAMERA_ONLY) != 0))
+    return KVC_ERR_INVALID_ARG;
+  return kvc_evict_frames(h, block, scale_frames, sliding_window);
 }
 
 int kvc_set_defer_eviction(kvc_handle* h, int32_t on) {
@@ -496,48 +564,74 @@ int kvc_clean(kvc_handle* h) {
 }
 
 int kvc_plan(kvc_handle* h, kvc_stream stream) {
+  NvtxRange range("kvc_plan");
   if (!h) return KVC_ERR_INVALID_ARG;
   const Block& b = h->blocks[0];
   const int32_t fpp = h->g.fpp;
   const int32_t s = b.special_frames;
-  const int32_t n_sp = (s + fpp - 1) / fpp;
-  const int32_t n_patch = b.scale.size + b.live.size;
-  const int32_t n_pages = n_patch + n_sp;
+  const int32_t n_scale = b.scale.size, n_live = b.live.size;
+  const int32_t n_patch = n_scale + n_live;
+  // Special-stream runs in frame positions: the frames of the scale pages are
+  // positions [0, n_scale) and the live frames [s - n_live, s), since frames
+  // enter the special stream in append order, eviction takes the oldest live
+  // frame and rollback the newest.  The default policy keeps every frame's
+  // specials; without cross-frame specials only those two runs are visible;
+  // camera_only adds the evicted frames' camera tokens, camera positions
+  // [n_scale, s - n_live).
+  kvc::PlanArgs& a = *h->plan_args;
+  a.n_runs = 0;
+  const int32_t evicted_lo = n_scale, evicted_hi = s - n_live;
+  if (h->cfg.special_policy == 0 || evicted_lo >= evicted_hi) {
+    a.runs[a.n_runs++] = kvc::PlanRun{h->g.P, fpp, kNumSpecial, 0, s};
+  } else {
+    a.runs[a.n_runs++] = kvc::PlanRun{h->g.P, fpp, kNumSpecial, 0, n_scale};
+    a.runs[a.n_runs++] = kvc::PlanRun{h->g.P, fpp, kNumSpecial, evicted_hi, s};
+    if (camera_stream(h->cfg))
+      a.runs[a.n_runs++] = kvc::PlanRun{h->g.first_camera, h->cfg.page_size, 1, evicted_lo, evicted_hi};
+  }
+  int32_t n_pages = n_patch;
+  for (int r = 0; r < a.n_runs; ++r) n_pages += kvc::run_pages(a.runs[r]);
   if (n_pages == 0) return KVC_ERR_EMPTY;
-  // Tokens in the last special page (compute_last_page_len).
-  const int32_t lpl = n_sp > 0 ? kNumSpecial * (s - fpp * (n_sp - 1)) : h->cfg.page_size;
+  if (n_pages > h->g.max_entries) return KVC_ERR_INVALID_ARG;
   const int kernel = h->device ? attn_kernel_for(h) : 1;
   if (kernel < 0) return KVC_ERR_INVALID_ARG;
   const int32_t tr = tile_rows_for(h, kernel);
-  // Tiles: ceil(valid / tile_rows) per visible page.
-  const int32_t full_sp = kNumSpecial * fpp;
-  int64_t n_tiles = (int64_t)n_patch * ((h->cfg.page_size + tr - 1) / tr);
-  if (n_sp > 0) n_tiles += (int64_t)(n_sp - 1) * ((full_sp + tr - 1) / tr) + (lpl + tr - 1) / tr;
-  if (n_tiles > h->g.L.max_tiles) return KVC_ERR_INVALID_ARG;
-  kvc::PlanArgs& a = *h->plan_args;
   a.n_patch = n_patch;
-  a.n_special = n_sp;
-  a.first_special = h->g.P;
-  a.full_special_len = full_sp;
-  a.last_page_len = lpl;
   a.page_size = h->cfg.page_size;
   a.tile_rows = tr;
-  for (int32_t i = 0; i < b.scale.size; ++i) a.patch_ids[i] = b.scale.at(i);
-  for (int32_t i = 0; i < b.live.size; ++i) a.patch_ids[b.scale.size + i] = b.live.at(i);
+  a.max_pages = h->g.max_pages;
+  for (int32_t i = 0; i < n_scale; ++i) a.patch_ids[i] = b.scale.at(i);
+  for (int32_t i = 0; i < n_live; ++i) a.patch_ids[n_scale + i] = b.live.at(i);
+  // Host copy of the visible entries (the device plan kernel writes the same).
+  int64_t n_tiles = 0;
+  int32_t e = 0;
+  for (; e < n_patch; ++e) {
+    h->plan_ids[e] = a.patch_ids[e];
+    h->plan_row0[e] = 0;
+    h->plan_valid[e] = h->cfg.page_size;
+    n_tiles += (h->cfg.page_size + tr - 1) / tr;
+  }
+  for (int r = 0; r < a.n_runs; ++r) {
+    const int32_t n = kvc::run_pages(a.runs[r]);
+    for (int32_t i = 0; i < n; ++i, ++e) {
+      kvc::run_entry(a.runs[r], i, &h->plan_ids[e], &h->plan_row0[e], &h->plan_valid[e]);
+      n_tiles += (h->plan_valid[e] + tr - 1) / tr;
+    }
+  }
+  if (n_tiles > h->g.L.max_tiles) return KVC_ERR_INVALID_ARG;
   if (h->device) {
     cudaError_t err = kvc::launch_plan(a, h->ws, h->g.L, (cudaStream_t)stream);
     if (err != cudaSuccess) return KVC_ERR_CUDA;
     ++h->launches;
   }
-  // Host copy of the plan and of the state it describes.
-  for (int32_t i = 0; i < n_patch; ++i) h->plan_ids[i] = a.patch_ids[i];
-  for (int32_t i = 0; i < n_sp; ++i) h->plan_ids[n_patch + i] = h->g.P + i;
   for (int32_t i = 0; i < n_patch; ++i) h->plan_snapshot[i] = a.patch_ids[i];
-  h->plan_n_scale = b.scale.size;
-  h->plan_n_live = b.live.size;
+  h->plan_n_scale = n_scale;
+  h->plan_n_live = n_live;
   h->plan_special_frames = s;
   h->plan_n_pages = n_pages;
-  h->plan_lpl = lpl;
+  // For the default policy this is compute_last_page_len: the last special
+  // page's tokens ([KVC] "Physical Page Layout and Indexing").
+  h->plan_lpl = h->plan_valid[n_pages - 1];
   h->plan_n_tiles = (int32_t)n_tiles;
   h->plan_tile_rows = tr;
   h->plan_kernel = kernel;
@@ -546,6 +640,7 @@ int kvc_plan(kvc_handle* h, kvc_stream stream) {
 }
 
 int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q, kvc_stream stream) {
+  NvtxRange range("kvc_run");
   int rc = check_run(h, block, Q, out, n_q);
   if (rc || n_q == 0) return rc;
   const int kernel = h->plan_kernel;
@@ -580,6 +675,7 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
 // with query rows [qo_indptr[r], qo_indptr[r+1]) of Q / out.
 int kvc_run_batch(kvc_handle* const* hs, const int32_t* blocks, int32_t count, const void* Q, void* out,
                   const int32_t* qo_indptr, kvc_stream stream) {
+  NvtxRange range("kvc_run_batch");
   if (!hs || !blocks || !qo_indptr || count < 1 || count > kvc::kTcMaxBatch) return KVC_ERR_INVALID_ARG;
   if (qo_indptr[0] != 0) return KVC_ERR_INVALID_ARG;
   for (int32_t r = 0; r < count; ++r) {
@@ -627,7 +723,8 @@ int kvc_run_batch(kvc_handle* const* hs, const int32_t* blocks, int32_t count, c
     const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
     if (h->cfg.max_kv_splits < max_s) max_s = h->cfg.max_kv_splits;
     if (h->plan_n_tiles > max_tiles) max_tiles = h->plan_n_tiles;
-    base += (int64_t)((n_q + kvc::kTcQRows - 1) / kvc::kTcQRows) * h->cfg.num_heads;
+    const int q_rows = 128 * q_tiles_for(h0);
+    base += (int64_t)((n_q + q_rows - 1) / q_rows) * h->cfg.num_heads;
   }
   if (max_s < 1) max_s = 1;
   int splits = 1;
@@ -735,6 +832,18 @@ int kvc_get_plan(const kvc_handle* h, int32_t* indptr2, int32_t* indices, int32_
   return KVC_OK;
 }
 
+int kvc_get_plan_ranges(const kvc_handle* h, int32_t* indices, int32_t* first_rows, int32_t* valid_lens,
+                        int32_t cap, int32_t* n_pages) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (!h->has_plan) return KVC_ERR_NO_PLAN;
+  if (n_pages) *n_pages = h->plan_n_pages;
+  if ((indices || first_rows || valid_lens) && cap < h->plan_n_pages) return KVC_ERR_INVALID_ARG;
+  if (indices) std::memcpy(indices, h->plan_ids, sizeof(int32_t) * h->plan_n_pages);
+  if (first_rows) std::memcpy(first_rows, h->plan_row0, sizeof(int32_t) * h->plan_n_pages);
+  if (valid_lens) std::memcpy(valid_lens, h->plan_valid, sizeof(int32_t) * h->plan_n_pages);
+  return KVC_OK;
+}
+
 int kvc_get_deques(const kvc_handle* h, int32_t block, int32_t* scale, int32_t* n_scale,
                    int32_t* live, int32_t* n_live, int32_t* free_list, int32_t* n_free) {
   int rc = check_block(h, block);
@@ -749,6 +858,24 @@ int kvc_get_deques(const kvc_handle* h, int32_t block, int32_t* scale, int32_t* 
   return KVC_OK;
 }
 
+int kvc_read_device_ranges(kvc_handle* h, int32_t* indices, int32_t* first_rows, int32_t* valid_lens,
+                           int32_t cap, int32_t* n_pages, kvc_stream stream) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (!h->device) return KVC_ERR_NO_DEVICE;
+  int32_t n = 0;
+  int rc = kvc_read_device_plan(h, indices, valid_lens, cap, &n, nullptr, stream);
+  if (rc) return rc;
+  if (n_pages) *n_pages = n;
+  if (first_rows && n > 0) {
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(first_rows, h->ws + h->g.L.page_row0, 4 * (size_t)n, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return KVC_ERR_CUDA;
+  }
+  return KVC_OK;
+}
+
 int kvc_read_device_plan(kvc_handle* h, int32_t* indices, int32_t* valid_lens, int32_t cap,
                          int32_t* n_pages, int32_t* last_page_len, kvc_stream stream) {
   if (!h) return KVC_ERR_INVALID_ARG;
@@ -760,7 +887,7 @@ int kvc_read_device_plan(kvc_handle* h, int32_t* indices, int32_t* valid_lens, i
     return KVC_ERR_CUDA;
   if (n_pages) *n_pages = hd.n_pages;
   if (last_page_len) *last_page_len = hd.last_page_len;
-  if (hd.n_pages < 0 || hd.n_pages > h->g.max_pages) return KVC_ERR_INVALID_ARG;
+  if (hd.n_pages < 0 || hd.n_pages > h->g.max_entries) return KVC_ERR_INVALID_ARG;
   if ((indices || valid_lens) && cap < hd.n_pages) return KVC_ERR_INVALID_ARG;
   if (hd.n_pages > 0) {
     if (indices && cudaMemcpyAsync(indices, h->ws + h->g.L.page_ids, 4 * (size_t)hd.n_pages,
@@ -786,7 +913,7 @@ int kvc_device_status(kvc_handle* h, kvc_stream stream) {
   if (cudaMemsetAsync(h->ws + h->g.L.status, 0, 256, st) != cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess)
     return KVC_ERR_CUDA;
-  return KVC_ERR_DEVICE_TIMEOUT;
+  return flag == kvc::kStatusBounds ? KVC_ERR_DEVICE_BOUNDS : KVC_ERR_DEVICE_TIMEOUT;
 }
 
 int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
@@ -801,6 +928,10 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
     case KVC_OPT_NUM_SPLITS:
       if (value < 0 || value > h->cfg.max_kv_splits) return KVC_ERR_INVALID_ARG;
       h->opt_splits = (int)value;
+      return KVC_OK;
+    case KVC_OPT_QUERY_TILES:
+      if (value < 0 || value > 2) return KVC_ERR_INVALID_ARG;
+      h->opt_qtiles = (int)value;
       return KVC_OK;
     case KVC_OPT_WAIT_BUDGET:
       if (value < 0) return KVC_ERR_INVALID_ARG;
@@ -864,6 +995,7 @@ const char* kvc_strerror(int code) {
     case KVC_ERR_EMPTY: return "no visible token";
     case KVC_ERR_NO_DEVICE: return "bookkeeping-only handle";
     case KVC_ERR_TOO_LARGE: return "too many pages or KV tiles for the static scratch array";
+    case KVC_ERR_DEVICE_BOUNDS: return "device bounds check failed (KVC_CHECKED build)";
     default: return "unknown error";
   }
 }

@@ -5,9 +5,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#ifdef __CUDACC__
+#define KVC_HD __host__ __device__
+#else
+#define KVC_HD
+#endif
+
+// KVC_CHECKED=1 builds (a separate library, libkvc_checked.so) add device-side
+// bounds checks on page ids, slots, tile rows and TMA coordinates; a failed
+// check records kStatusBounds, where and the bad value in the status word and
+// skips the access -- it never traps.
+#ifndef KVC_CHECKED
+#define KVC_CHECKED 0
+#endif
+
 namespace kvc {
 
 constexpr int kNumSpecial = 6;
+constexpr int32_t kStatusTimeout = 1;   // status[0]: a bounded wait ran out
+constexpr int32_t kStatusBounds = 2;    // status[0]: a bounds check failed (checked builds)
+
+#ifdef __CUDACC__
+// First failure wins: status = {code, where, value}.
+__device__ inline void record_bounds(int32_t* status, int32_t where, int32_t value) {
+  if (atomicCAS(status, 0, kStatusBounds) == 0) {
+    status[1] = where;
+    status[2] = value;
+  }
+  __threadfence();
+}
+#endif
 constexpr int kMaxPatchPages = 1024;   // bound on P (the patch pool), kernel-argument sized
 
 // Device plan written by the plan kernel into the workspace.
@@ -32,6 +59,7 @@ struct WorkspaceLayout {
   size_t header;       // DevPlanHeader
   size_t page_ids;     // int32[max_pages]
   size_t page_valid;   // int32[max_pages]
+  size_t page_row0;    // int32[max_pages]: first visible row of each visible page
   size_t tiles;        // KvTile[max_tiles]
   size_t part_o;       // float[max_splits][max_q][H][D]
   size_t part_lse;     // float[max_splits][max_q][H]
@@ -40,15 +68,40 @@ struct WorkspaceLayout {
   int32_t max_tiles;
 };
 
+// A run of consecutive positions [a, b) of an append-only stream whose page
+// p (id page0 + p) holds positions [p * per_page, (p + 1) * per_page), `tok`
+// rows each: the special stream (6 rows per frame) or the camera stream (one
+// row per frame).  A run covers pages floor(a / per_page) ..
+// ceil(b / per_page) - 1; its first and last page may be partial.
+struct PlanRun {
+  int32_t page0, per_page, tok, a, b;
+};
+
+KVC_HD inline int32_t run_pages(const PlanRun& r) {
+  return r.b > r.a ? (r.b + r.per_page - 1) / r.per_page - r.a / r.per_page : 0;
+}
+// Page id, first row and row count of page e of the run.
+KVC_HD inline void run_entry(const PlanRun& r, int32_t e, int32_t* page, int32_t* row0, int32_t* rows) {
+  const int32_t p = r.a / r.per_page + e;
+  const int32_t lo = r.a > p * r.per_page ? r.a : p * r.per_page;
+  const int32_t hi = r.b < (p + 1) * r.per_page ? r.b : (p + 1) * r.per_page;
+  *page = r.page0 + p;
+  *row0 = r.tok * (lo - p * r.per_page);
+  *rows = r.tok * (hi - lo);
+}
+
+constexpr int kMaxRuns = 3;
+
 // Arguments of the plan kernel, passed by value (no host->device copy).
+// Visible entries: the n_patch patch pages (all rows), then every page of
+// each run in order.
 struct PlanArgs {
   int32_t n_patch;                  // visible patch pages (scale + live)
-  int32_t n_special;                // visible special pages
-  int32_t first_special;            // page id of the first special page (= P)
-  int32_t full_special_len;         // valid tokens of a non-last special page (6*fpp)
-  int32_t last_page_len;            // valid tokens of the last special page
+  int32_t n_runs;                   // special / camera runs
+  PlanRun runs[kMaxRuns];
   int32_t page_size;
   int32_t tile_rows;                // rows per KV tile of the attention kernel
+  int32_t max_pages;                // pages of one block's cache (bounds checks)
   int32_t patch_ids[kMaxPatchPages];
 };
 
@@ -66,6 +119,7 @@ struct AttnArgs {
   int32_t page_size;
   int32_t n_tiles;
   int32_t n_splits;
+  int32_t max_pages;      // pages of one block's cache (bounds checks)
   float sm_scale_log2;    // sm_scale * log2(e)
   long long wait_budget;  // clock cycles per bounded wait
   int32_t stall_test;     // 1: wait once on a barrier nothing signals (timeout test)
@@ -73,8 +127,9 @@ struct AttnArgs {
 
 // kvc_kernels.cu
 cudaError_t launch_append(void* cache_block, const void* K, const void* V, int32_t page,
-                          int32_t special_page, int32_t special_slot, int32_t page_size,
-                          int64_t row_bytes, cudaStream_t stream);
+                          int32_t special_page, int32_t special_slot, int32_t camera_page,
+                          int32_t camera_slot, int32_t page_size, int64_t row_bytes, int32_t max_pages,
+                          int32_t* status, cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, void* workspace, const WorkspaceLayout& L,
                         cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnArgs& a, int dtype, cudaStream_t stream);
@@ -84,7 +139,7 @@ int simt_tile_rows(int head_dim);
 // kvc_attn_tc.cu
 bool tc_supported(int dtype, int head_dim, int num_heads, int page_size);
 constexpr int kTcTileRows = 128;
-constexpr int kTcQRows = 256;   // query rows per CTA of the tensor-core kernel
+constexpr int kTcQRows = 256;   // most query rows per CTA of the tensor-core kernel
 struct TcMaps;   // opaque: TMA descriptors of the cache (per handle)
 TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, int page_size,
                        int num_heads, int head_dim, cudaError_t* err);
@@ -95,7 +150,7 @@ void tc_destroy_maps(TcMaps* m);
 constexpr int kTcMaxBatch = 16;
 struct TcRequestDesc {
   TcMaps* maps;
-  int32_t block, max_pages;
+  int32_t block, max_pages, page_size;
   const KvTile* tiles;
   float* part_o;          // [n_splits][n_q][H][D] (n_splits > 1)
   float* part_lse;        // [n_splits][n_q][H]
@@ -107,6 +162,7 @@ struct TcBatchArgs {
   void* out;
   int32_t rows, num_heads, head_dim, dtype, stall_test, count;
   int32_t num_sms;        // of the device: decides whether a launch has several waves
+  int32_t q_tiles;        // 128-row query tiles per CTA: 2, or 1 (both softmax groups on one tile)
   float sm_scale_log2;
   long long wait_budget;
   TcRequestDesc req[kTcMaxBatch];

@@ -23,18 +23,32 @@ namespace {
 // One frame's K/V [6 + ps, H, D]: rows 0..5 (camera, 4 registers, scale) go to
 // slots [special_slot, +6) of the special page, rows 6.. fill the patch page
 // ([SLOTS] "双流分页布局", "特殊 token 流"; [KVC] "Append and Evict API").
-// grid = (ceil(row16 / blockDim), 2 * (6 + ps)); one thread moves 16 bytes.
+// With a camera stream (camera_page >= 0), row 0 is also copied to row
+// camera_slot of the camera page.
+// grid = (ceil(row16 / blockDim), 2 * (6 + ps + cam)); one thread moves 16 bytes.
 __global__ void append_kernel(char* __restrict__ cache_block, const char* __restrict__ K,
                               const char* __restrict__ V, int32_t page, int32_t special_page,
-                              int32_t special_slot, int32_t page_size, int64_t row_bytes) {
+                              int32_t special_slot, int32_t camera_page, int32_t camera_slot,
+                              int32_t page_size, int64_t row_bytes, int32_t max_pages,
+                              int32_t* __restrict__ status) {
   const int32_t T = kNumSpecial + page_size;
-  const int32_t kv = blockIdx.y / T;
-  const int32_t r = blockIdx.y - kv * T;
+  if (KVC_CHECKED && (page < 0 || page >= max_pages || special_page < 0 || special_page >= max_pages ||
+                      special_slot < 0 || special_slot + kNumSpecial > page_size ||
+                      (camera_page >= 0 && (camera_page >= max_pages || camera_slot < 0 ||
+                                            camera_slot >= page_size)))) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) record_bounds(status, 101, page);
+    return;
+  }
+  const int32_t rows = T + (camera_page >= 0 ? 1 : 0);
+  const int32_t kv = blockIdx.y / rows;
+  const int32_t r = blockIdx.y - kv * rows;
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (c * 16 >= row_bytes) return;
-  const char* src = (kv ? V : K) + (int64_t)r * row_bytes + c * 16;
+  const char* src = (kv ? V : K) + (int64_t)(r < T ? r : 0) * row_bytes + c * 16;
   int64_t dst_row;
-  if (r < kNumSpecial)
+  if (r == T)
+    dst_row = ((int64_t)camera_page * 2 + kv) * page_size + camera_slot;
+  else if (r < kNumSpecial)
     dst_row = ((int64_t)special_page * 2 + kv) * page_size + special_slot + r;
   else
     dst_row = ((int64_t)page * 2 + kv) * page_size + (r - kNumSpecial);
@@ -43,48 +57,70 @@ __global__ void append_kernel(char* __restrict__ cache_block, const char* __rest
 }
 
 // ------------------------------------------------------------------- plan
-// Visible order: scale pages, live window, then every special page; a
-// non-last special page holds 6*fpp valid tokens, the last last_page_len
-// ([KVC] "Patch Pages vs. Special Pages"; [SLOTS] "双流分页布局").
+// Visible order: scale pages, live window, then the pages of the special
+// (and camera) runs; every page contributes rows [row0, row0 + valid)
+// ([KVC] "Patch Pages vs. Special Pages"; [SLOTS] "双流分页布局").  With the
+// default special policy there is one run, every special page from row 0, a
+// non-last page holding 6*fpp tokens and the last last_page_len.
 __global__ void plan_kernel(const __grid_constant__ PlanArgs a, char* __restrict__ ws,
                             WorkspaceLayout L) {
-  const int32_t n_pages = a.n_patch + a.n_special;
   const int32_t tr = a.tile_rows;
   const int32_t tpp = (a.page_size + tr - 1) / tr;
-  const int32_t tps = (a.full_special_len + tr - 1) / tr;
   int32_t* ids = reinterpret_cast<int32_t*>(ws + L.page_ids);
   int32_t* valid = reinterpret_cast<int32_t*>(ws + L.page_valid);
+  int32_t* first = reinterpret_cast<int32_t*>(ws + L.page_row0);
   KvTile* tiles = reinterpret_cast<KvTile*>(ws + L.tiles);
-  for (int32_t i = threadIdx.x; i < n_pages; i += blockDim.x) {
-    const bool patch = i < a.n_patch;
-    const int32_t j = i - a.n_patch;
-    const int32_t id = patch ? a.patch_ids[i] : a.first_special + j;
-    const int32_t v = patch ? a.page_size : (i == n_pages - 1 ? a.last_page_len : a.full_special_len);
-    const int32_t tile0 = patch ? i * tpp : a.n_patch * tpp + j * tps;
-    const int32_t token0 = patch ? i * a.page_size : a.n_patch * a.page_size + j * a.full_special_len;
+  auto emit = [&](int32_t i, int32_t id, int32_t row0, int32_t v, int32_t tile0, int32_t token0) {
+    if (KVC_CHECKED && (i < 0 || i >= L.max_pages || id < 0 || id >= a.max_pages || row0 < 0 || v < 1 ||
+                        row0 + v > a.page_size || tile0 < 0 || tile0 + (v + tr - 1) / tr > L.max_tiles)) {
+      record_bounds(reinterpret_cast<int32_t*>(ws + L.status), 201, i);
+      return;
+    }
     ids[i] = id;
     valid[i] = v;
-    for (int32_t t = 0, r0 = 0; r0 < v; ++t, r0 += tr) {
+    first[i] = row0;
+    for (int32_t t = 0, r = 0; r < v; ++t, r += tr) {
       KvTile k;
       k.page = id;
-      k.row0 = r0;
-      k.rows = min(tr, v - r0);
-      k.token0 = token0 + r0;
+      k.row0 = row0 + r;
+      k.rows = min(tr, v - r);
+      k.token0 = token0 + r;
       tiles[tile0 + t] = k;
     }
+  };
+  for (int32_t i = threadIdx.x; i < a.n_patch; i += blockDim.x)
+    emit(i, a.patch_ids[i], 0, a.page_size, i * tpp, i * a.page_size);
+  // Runs: page e of a run starts after the run's earlier pages; only a run's
+  // first and last page can be partial, so the offsets have a closed form.
+  int32_t entry = a.n_patch, tile = a.n_patch * tpp, token = a.n_patch * a.page_size;
+  int32_t last_valid = a.n_patch > 0 ? a.page_size : 0;
+  for (int32_t r = 0; r < a.n_runs; ++r) {
+    const PlanRun& run = a.runs[r];
+    const int32_t n = run_pages(run);
+    int32_t id, row0, v0, vf, vl;
+    run_entry(run, 0, &id, &row0, &v0);
+    run_entry(run, n > 1 ? 1 : 0, &id, &row0, &vf);
+    run_entry(run, n - 1, &id, &row0, &vl);
+    const int32_t t0 = (v0 + tr - 1) / tr, tf = (vf + tr - 1) / tr;
+    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
+      int32_t v;
+      run_entry(run, e, &id, &row0, &v);
+      emit(entry + e, id, row0, v, tile + (e == 0 ? 0 : t0 + (e - 1) * tf),
+           token + (e == 0 ? 0 : v0 + (e - 1) * vf));
+    }
+    if (n > 0) {
+      tile += n == 1 ? t0 : t0 + (n - 2) * tf + (vl + tr - 1) / tr;
+      token += n == 1 ? v0 : v0 + (n - 2) * vf + vl;
+      last_valid = vl;
+    }
+    entry += n;
   }
   if (threadIdx.x == 0) {
     DevPlanHeader h;
-    h.n_pages = n_pages;
-    h.last_page_len = a.last_page_len;
-    int32_t n_tiles = a.n_patch * tpp;
-    int32_t n_tokens = a.n_patch * a.page_size;
-    if (a.n_special > 0) {
-      n_tiles += (a.n_special - 1) * tps + (a.last_page_len + tr - 1) / tr;
-      n_tokens += (a.n_special - 1) * a.full_special_len + a.last_page_len;
-    }
-    h.n_tiles = n_tiles;
-    h.n_tokens = n_tokens;
+    h.n_pages = entry;
+    h.last_page_len = last_valid;
+    h.n_tiles = tile;
+    h.n_tokens = token;
     *reinterpret_cast<DevPlanHeader*>(ws + L.header) = h;
   }
 }
@@ -131,6 +167,11 @@ attn_simt_kernel(const AttnArgs a) {
   const T* cache = reinterpret_cast<const T*>(a.cache);
   for (int t = t0; t < t1; ++t) {
     const KvTile tile = a.tiles[t];
+    if (KVC_CHECKED && (tile.page < 0 || tile.page >= a.max_pages || tile.row0 < 0 || tile.rows < 1 ||
+                        tile.rows > BN || tile.row0 + tile.rows > a.page_size)) {
+      if (threadIdx.x == 0) record_bounds(a.status, 301, t);
+      continue;                                        // uniform over the CTA: skip the tile
+    }
     const int64_t kbase = (((int64_t)tile.page * 2 + 0) * a.page_size + tile.row0) * row_elems + (int64_t)h * D;
     const int64_t vbase = (((int64_t)tile.page * 2 + 1) * a.page_size + tile.row0) * row_elems + (int64_t)h * D;
     for (int idx = threadIdx.x; idx < tile.rows * D; idx += kSimtThreads) {
@@ -279,14 +320,17 @@ cudaError_t merge_by_dim(const AttnArgs& a, cudaStream_t st) {
 int simt_tile_rows(int head_dim) { return head_dim >= 128 ? 32 : 64; }
 
 cudaError_t launch_append(void* cache_block, const void* K, const void* V, int32_t page,
-                          int32_t special_page, int32_t special_slot, int32_t page_size,
-                          int64_t row_bytes, cudaStream_t stream) {
+                          int32_t special_page, int32_t special_slot, int32_t camera_page,
+                          int32_t camera_slot, int32_t page_size, int64_t row_bytes, int32_t max_pages,
+                          int32_t* status, cudaStream_t stream) {
   const int64_t row16 = row_bytes / 16;
   const int threads = row16 >= 128 ? 128 : (int)((row16 + 31) / 32 * 32);
-  dim3 grid((unsigned)((row16 + threads - 1) / threads), 2u * (unsigned)(kNumSpecial + page_size));
+  const unsigned rows = (unsigned)(kNumSpecial + page_size + (camera_page >= 0 ? 1 : 0));
+  dim3 grid((unsigned)((row16 + threads - 1) / threads), 2u * rows);
   append_kernel<<<grid, threads, 0, stream>>>(static_cast<char*>(cache_block),
                                              static_cast<const char*>(K), static_cast<const char*>(V),
-                                             page, special_page, special_slot, page_size, row_bytes);
+                                             page, special_page, special_slot, camera_page, camera_slot,
+                                             page_size, row_bytes, max_pages, status);
   return cudaGetLastError();
 }
 

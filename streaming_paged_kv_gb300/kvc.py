@@ -12,9 +12,13 @@ streams), creates the handle and forwards torch tensors' pointers.
 
 import ctypes
 import os
+import sys
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libkvc.so")
+# KVC_CHECKED=1 selects the build with device-side bounds checks; KVC_LIB names
+# another build of the same library (the sanitizer test's host build).
+LIB_PATH = os.environ.get("KVC_LIB") or os.path.join(
+    _PKG, "libkvc_checked.so" if os.environ.get("KVC_CHECKED") == "1" else "libkvc.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run streaming_paged_kv_gb300.build.build()")
 lib = ctypes.CDLL(LIB_PATH)
@@ -26,8 +30,16 @@ ERRORS = {
     0: "OK", -1: "INVALID_ARG", -2: "NO_FREE_PAGE", -3: "SPECIAL_POOL_FULL",
     -4: "NOTHING_TO_ROLLBACK", -5: "ROLLBACK_AFTER_EVICT", -6: "NO_PLAN", -7: "STALE_PLAN",
     -8: "CUDA", -9: "DEVICE_TIMEOUT", -10: "EMPTY", -11: "NO_DEVICE", -12: "TOO_LARGE",
+    -13: "DEVICE_BOUNDS",
 }
 KVC_OPT_ATTN_KERNEL, KVC_OPT_NUM_SPLITS, KVC_OPT_WAIT_BUDGET, KVC_OPT_TIMING, KVC_OPT_STALL_TEST = 1, 2, 3, 4, 5
+KVC_OPT_QUERY_TILES = 6
+
+try:
+    _DEBUG_EVERY = max(0, int(os.environ.get("KVC_DEBUG", "0") or 0))   # see PagedKVCache.plan
+except ValueError:
+    _DEBUG_EVERY = 0
+KVC_SPECIAL_NO_CROSS_FRAME, KVC_SPECIAL_CAMERA_ONLY = 1, 2
 
 
 class kvc_config(ctypes.Structure):
@@ -38,7 +50,7 @@ class kvc_config(ctypes.Structure):
         ("sliding_window", ctypes.c_int32), ("headroom", ctypes.c_int32),
         ("max_total_frames", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("sm_scale", ctypes.c_float), ("max_query_tokens", ctypes.c_int32),
-        ("max_kv_splits", ctypes.c_int32),
+        ("max_kv_splits", ctypes.c_int32), ("special_policy", ctypes.c_int32),
     ]
 
 
@@ -55,6 +67,14 @@ class KvcError(RuntimeError):
         super().__init__(f"{call}: {self.code} ({msg})" if call else f"{self.code} ({msg})")
 
 
+class Geometry(ctypes.Structure):
+    _fields_ = [("num_patch_pages", ctypes.c_int32), ("frames_per_special_page", ctypes.c_int32),
+                ("num_special_pages", ctypes.c_int32), ("num_camera_pages", ctypes.c_int32),
+                ("max_num_pages", ctypes.c_int32),
+                ("tokens_per_frame", ctypes.c_int32), ("page_bytes", ctypes.c_int64),
+                ("block_bytes", ctypes.c_int64)]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -62,10 +82,12 @@ _PI32 = ctypes.POINTER(ctypes.c_int32)
 _SIGS = {
     "kvc_required_bytes": [ctypes.POINTER(kvc_config), ctypes.POINTER(ctypes.c_size_t),
                            ctypes.POINTER(ctypes.c_size_t)],
+    "kvc_get_geometry": [ctypes.POINTER(kvc_config), ctypes.POINTER(Geometry)],
     "kvc_create": [ctypes.POINTER(kvc_config), _P, _P, _P, ctypes.POINTER(_P)],
     "kvc_destroy": [_P],
     "kvc_append_frame": [_P, _I32, _P, _P, _P],
     "kvc_evict_frames": [_P, _I32, _I32, _I32],
+    "kvc_evict_frames_ex": [_P, _I32, _I32, _I32, _I32, _I32],
     "kvc_set_defer_eviction": [_P, _I32],
     "kvc_execute_deferred_eviction": [_P, _I32, _I32, _I32],
     "kvc_rollback_last_frame": [_P, _I32],
@@ -76,6 +98,8 @@ _SIGS = {
     "kvc_run_batch": [ctypes.POINTER(_P), _PI32, _I32, _P, _P, _PI32, _P],
     "kvc_get_cache_stats": [_P, _I32, ctypes.POINTER(kvc_stats)],
     "kvc_get_plan": [_P, _PI32, _PI32, _I32, _PI32, _PI32],
+    "kvc_get_plan_ranges": [_P, _PI32, _PI32, _PI32, _I32, _PI32],
+    "kvc_read_device_ranges": [_P, _PI32, _PI32, _PI32, _I32, _PI32, _P],
     "kvc_get_deques": [_P, _I32, _PI32, _PI32, _PI32, _PI32, _PI32, _PI32],
     "kvc_read_device_plan": [_P, _PI32, _PI32, _I32, _PI32, _PI32, _P],
     "kvc_device_status": [_P, _P],
@@ -99,13 +123,20 @@ def _check(rc, call):
     return rc
 
 
+def special_policy(cross_frame_special=True, camera_only=False):
+    """kvc_config.special_policy for the two eviction options."""
+    return (0 if cross_frame_special else KVC_SPECIAL_NO_CROSS_FRAME) | \
+        (KVC_SPECIAL_CAMERA_ONLY if camera_only else 0)
+
+
 def make_config(num_blocks, num_heads, head_dim, page_size, dtype="bf16", scale_frames=8,
                 sliding_window=64, headroom=16, max_total_frames=2048, sm_scale=0.0,
-                max_query_tokens=0, max_kv_splits=0):
+                max_query_tokens=0, max_kv_splits=0, cross_frame_special=True, camera_only=False):
     """kvc_config with the pages' defaults (8 / 64 / 16 / 2048)."""
     return kvc_config(num_blocks, num_heads, head_dim, page_size, 6, scale_frames,
                       sliding_window, headroom, max_total_frames, DTYPE_CODE[dtype],
-                      float(sm_scale), max_query_tokens, max_kv_splits)
+                      float(sm_scale), max_query_tokens, max_kv_splits,
+                      special_policy(cross_frame_special, camera_only))
 
 
 # ----------------------------------------------------- same-name wrappers
@@ -114,6 +145,12 @@ def kvc_required_bytes(cfg):
     _check(lib.kvc_required_bytes(ctypes.byref(cfg), ctypes.byref(c), ctypes.byref(w)),
            "kvc_required_bytes")
     return c.value, w.value
+
+
+def kvc_get_geometry(cfg):
+    g = Geometry()
+    _check(lib.kvc_get_geometry(ctypes.byref(cfg), ctypes.byref(g)), "kvc_get_geometry")
+    return g
 
 
 def kvc_create(cfg, cache_ptr=None, workspace_ptr=None, stream=None):
@@ -133,6 +170,11 @@ def kvc_append_frame(h, block, k_ptr, v_ptr, stream=None):
 
 def kvc_evict_frames(h, block, scale_frames, sliding_window):
     return _check(lib.kvc_evict_frames(h, block, scale_frames, sliding_window), "kvc_evict_frames")
+
+
+def kvc_evict_frames_ex(h, block, scale_frames, sliding_window, cross_frame_special, camera_only):
+    return _check(lib.kvc_evict_frames_ex(h, block, scale_frames, sliding_window, int(bool(cross_frame_special)),
+                                          int(bool(camera_only))), "kvc_evict_frames_ex")
 
 
 def kvc_set_defer_eviction(h, on):
@@ -200,6 +242,21 @@ def kvc_get_plan(h, cap=4096):
     return list(idx[:n.value]), [indptr[0], indptr[1]], lpl.value
 
 
+def kvc_get_plan_ranges(h, cap=8192):
+    bufs = [(ctypes.c_int32 * cap)() for _ in range(3)]
+    n = ctypes.c_int32()
+    _check(lib.kvc_get_plan_ranges(h, bufs[0], bufs[1], bufs[2], cap, ctypes.byref(n)), "kvc_get_plan_ranges")
+    return tuple(list(b[:n.value]) for b in bufs)
+
+
+def kvc_read_device_ranges(h, stream=None, cap=8192):
+    bufs = [(ctypes.c_int32 * cap)() for _ in range(3)]
+    n = ctypes.c_int32()
+    _check(lib.kvc_read_device_ranges(h, bufs[0], bufs[1], bufs[2], cap, ctypes.byref(n), stream),
+           "kvc_read_device_ranges")
+    return tuple(list(b[:n.value]) for b in bufs)
+
+
 def kvc_get_deques(h, block, cap=1024):
     bufs = [(ctypes.c_int32 * cap)() for _ in range(3)]
     ns = [ctypes.c_int32() for _ in range(3)]
@@ -261,18 +318,22 @@ class PagedKVCache:
 
     def __init__(self, num_blocks, num_heads, head_dim, page_size, dtype="bf16", scale_frames=8,
                  sliding_window=64, headroom=16, max_total_frames=2048, sm_scale=0.0,
-                 max_query_tokens=0, max_kv_splits=0, device="cuda"):
+                 max_query_tokens=0, max_kv_splits=0, device="cuda", cross_frame_special=True,
+                 camera_only=False):
         self.cfg = make_config(num_blocks, num_heads, head_dim, page_size, dtype, scale_frames,
                                sliding_window, headroom, max_total_frames, sm_scale,
-                               max_query_tokens, max_kv_splits)
+                               max_query_tokens, max_kv_splits, cross_frame_special, camera_only)
+        self.cross_frame_special, self.camera_only = bool(cross_frame_special), bool(camera_only)
         self.dtype = dtype
         self.num_blocks, self.num_heads, self.head_dim = num_blocks, num_heads, head_dim
         self.page_size = page_size
         self.scale_frames, self.sliding_window = scale_frames, sliding_window
-        self.num_patch_pages = scale_frames + sliding_window + headroom
-        self.frames_per_special_page = page_size // 6
-        self.num_special_pages = -(-max_total_frames // self.frames_per_special_page)
-        self.max_num_pages = self.num_patch_pages + self.num_special_pages
+        geo = kvc_get_geometry(self.cfg)          # the library's page geometry
+        self.num_patch_pages = geo.num_patch_pages
+        self.frames_per_special_page = geo.frames_per_special_page
+        self.num_special_pages = geo.num_special_pages
+        self.num_camera_pages = geo.num_camera_pages
+        self.max_num_pages = geo.max_num_pages
         self.cache_bytes, self.workspace_bytes = kvc_required_bytes(self.cfg)
         self.device = device
         self.cache = self.workspace = None
@@ -310,9 +371,16 @@ class PagedKVCache:
     def append_frame(self, block, k=None, v=None):
         kvc_append_frame(self.h, block, self._ptr(k), self._ptr(v), self._stream())
 
-    def evict_frames(self, block, scale_frames=None, sliding_window=None):
-        kvc_evict_frames(self.h, block, self.scale_frames if scale_frames is None else scale_frames,
-                         self.sliding_window if sliding_window is None else sliding_window)
+    def evict_frames(self, block, scale_frames=None, sliding_window=None, cross_frame_special=None,
+                     camera_only=None):
+        sf = self.scale_frames if scale_frames is None else scale_frames
+        sw = self.sliding_window if sliding_window is None else sliding_window
+        if cross_frame_special is None and camera_only is None:
+            kvc_evict_frames(self.h, block, sf, sw)
+        else:
+            kvc_evict_frames_ex(self.h, block, sf, sw,
+                                self.cross_frame_special if cross_frame_special is None else cross_frame_special,
+                                self.camera_only if camera_only is None else camera_only)
 
     def set_defer_eviction(self, on):
         kvc_set_defer_eviction(self.h, on)
@@ -330,6 +398,17 @@ class PagedKVCache:
 
     def plan(self):
         kvc_plan(self.h, self._stream())
+        if _DEBUG_EVERY:
+            # KVC_DEBUG=N: every N plans (one per streamed frame) print each
+            # block's slot usage, like the pages' LINGBOT_DEBUG_KV ([SLOTS]
+            # "动手验证"): scale_pg / live_pg / free_pg / special.
+            self._plans = getattr(self, "_plans", 0) + 1
+            if self._plans % _DEBUG_EVERY == 0:
+                for b in range(self.num_blocks):
+                    st = self.stats(b)
+                    print(f"[kvc] frame {st['frame_count']} block {b}: scale_pg={st['scale_pages']} "
+                          f"live_pg={st['live_pages']} free_pg={st['free_pages']} "
+                          f"special={st['special_tokens']}", file=sys.stderr)
 
     def run(self, block, q, out):
         kvc_run(self.h, block, self._ptr(q), self._ptr(out), q.shape[0], self._stream())
@@ -350,6 +429,10 @@ class PagedKVCache:
 
     def plan_table(self):
         return kvc_get_plan(self.h)
+
+    def plan_ranges(self):
+        """(indices, first_rows, valid_lens) of the current plan (host copy)."""
+        return kvc_get_plan_ranges(self.h)
 
     def deques(self, block):
         return kvc_get_deques(self.h, block)

@@ -25,17 +25,22 @@ class ParityEngine:
     request."""
 
     def __init__(self, kvc, w, seed=0, check_frames=(), kernel=0, splits=0, rows=None,
-                 check_bytes=False, check_device_plan=False, mirror_blocks=None):
+                 check_bytes=False, check_device_plan=False, mirror_blocks=None, qtiles=0,
+                 cross_frame_special=True, camera_only=False):
         self.kvc, self.w, self.seed = kvc, w, seed
+        self.policy = dict(cross_frame_special=cross_frame_special, camera_only=camera_only)
         self.c = kvc.PagedKVCache(w.num_layers, w.num_heads, w.head_dim, w.page_size, w.dtype,
-                                  w.scale_frames, w.sliding_window, w.headroom, w.max_total_frames)
+                                  w.scale_frames, w.sliding_window, w.headroom, w.max_total_frames,
+                                  **self.policy)
         if kernel:
             self.c.set_option(kvc.KVC_OPT_ATTN_KERNEL, kernel)
         if splits:
             self.c.set_option(kvc.KVC_OPT_NUM_SPLITS, splits)
+        if qtiles:
+            self.c.set_option(kvc.KVC_OPT_QUERY_TILES, qtiles)
         self.orc = OraclePagedKV(w.num_layers, w.page_size, w.num_heads, w.head_dim, w.dtype,
                                  w.scale_frames, w.sliding_window, w.headroom, w.max_total_frames,
-                                 mirror_blocks=mirror_blocks)
+                                 mirror_blocks=mirror_blocks, **self.policy)
         self.head_scale = k_head_scale(seed, w.wid, w.num_heads) if w.k_head_scale else None
         self.check_frames = set(check_frames)
         self.rows = rows
@@ -60,8 +65,11 @@ class ParityEngine:
                                   np.empty(k.shape, np.uint16 if self.w.dtype != "f32" else np.uint32))
 
     def evict(self, b):
-        self.c.evict_frames(b)
-        self.orc.evict_frames(b, self.w.scale_frames, self.w.sliding_window)
+        if self.policy["cross_frame_special"] and not self.policy["camera_only"]:
+            self.c.evict_frames(b)
+        else:
+            self.c.evict_frames(b, **self.policy)         # kvc_evict_frames_ex
+        self.orc.evict_frames(b, self.w.scale_frames, self.w.sliding_window, **self.policy)
 
     def set_defer(self, on):
         self.c.set_defer_eviction(on)
@@ -85,6 +93,9 @@ class ParityEngine:
             idx, valid, lpl = self.kvc.kvc_read_device_plan(self.c.h, self.c._stream())
             o_idx, _, o_lpl, o_valid = self.orc.visible_page_table(0)
             assert (idx, valid, lpl) == (o_idx, o_valid, o_lpl)
+            want = tuple(self.orc.visible_ranges(0))
+            assert tuple(self.kvc.kvc_read_device_ranges(self.c.h, self.c._stream())) == want
+            assert tuple(self.c.plan_ranges()) == want
 
     def attend(self, b, f):
         q = self._q[b]

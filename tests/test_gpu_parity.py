@@ -122,6 +122,70 @@ def test_split_counts(kvc, kernel, splits):
     e.close()
 
 
+@pytest.mark.parametrize("qtiles", [1, 2])
+@pytest.mark.parametrize("splits", [1, 3, 7])
+def test_query_tiles_per_cta(kvc, qtiles, splits):
+    """Tensor-core kernel with one 128-row query tile per CTA (both softmax
+    warp groups on alternate KV tiles of it) and with two: a 224x224 frame
+    (262 rows: two full tiles and a 6-row tail) through the first eviction,
+    with partial special pages."""
+    w = WORKLOADS["s224"].with_(num_layers=1, n_frames=75)
+    _kernel_or_skip(kvc, w, 2)
+    e = ParityEngine(kvc, w, check_frames={0, 1, 9, 43, 74}, kernel=2, splits=splits, qtiles=qtiles)
+    drive(w, e)
+    mx, rel = e.worst()
+    assert mx <= 2e-2 and rel <= 5e-3, e.results
+    e.close()
+
+
+@pytest.mark.parametrize("qtiles", [1, 2])
+def test_one_tile_splits(kvc, qtiles):
+    """One KV split per tile (7 tiles: 3 pages x 2 + the 18-row special tile),
+    with one and two query tiles per CTA: CTAs whose split is a single short
+    tile, and splits of 1 and 3."""
+    from oracle import OraclePagedKV, paged_attention
+    from streaming_paged_kv_gb300.inputs import frame_qkv, to_bits
+    c = kvc.PagedKVCache(1, 16, 64, 256, "bf16", max_total_frames=64, max_kv_splits=16)
+    try:
+        c.set_option(kvc.KVC_OPT_ATTN_KERNEL, 2)
+    except kvc.KvcError:
+        c.close()
+        pytest.skip("no tensor-core kernel")
+    orc = OraclePagedKV(1, 256, 16, 64, "bf16", 8, 64, 16, 64)
+    for f in range(3):
+        q, k, v = frame_qkv(21, 2, f, 0, 256, 16, 64)
+        c.append_frame(0, k.cuda(), v.cuda())
+        orc.append_frame(0, to_bits(k), to_bits(v))
+    c.plan()
+    c.set_option(kvc.KVC_OPT_QUERY_TILES, qtiles)
+    want = paged_attention(orc, 0, to_bits(q))
+    for splits in (7, 1, 3):                     # 3 pages x 2 tiles + 1 special tile = 7 tiles
+        c.set_option(kvc.KVC_OPT_NUM_SPLITS, splits)
+        qd = q.cuda()
+        out = torch.empty_like(qd)
+        c.run(0, qd, out)
+        torch.cuda.synchronize()
+        mx, rel = compare(out, want, "bf16")
+        assert mx <= 2e-2 and rel <= 5e-3, (splits, mx, rel)
+    assert kvc.kvc_device_status(c.h, c._stream()) == 0
+    c.close()
+
+
+@pytest.mark.parametrize("qtiles", [1, 2])
+def test_s518_ragged_query_tiles(kvc, qtiles):
+    """The 518x378 page geometry (999-row pages: ragged 103-row KV tiles; 1005
+    query rows: a 109-row last query tile) with one and two query tiles per CTA."""
+    w = WORKLOADS["s518"].with_(num_layers=1, n_frames=12, sliding_window=4, headroom=2,
+                                max_total_frames=400)
+    _kernel_or_skip(kvc, w, 2)
+    rows = list(range(0, 1005, 5)) + [1004]
+    e = ParityEngine(kvc, w, check_frames={0, 6, 11}, kernel=2, rows=rows, qtiles=qtiles)
+    drive(w, e)
+    mx, rel = e.worst()
+    assert mx <= 2e-2 and rel <= 5e-3, e.results
+    e.close()
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_s518_exact_pages_ragged(kvc, kernel):
     # page_size 999: 7 full 128-row tiles + a 103-row tail per patch page;

@@ -21,13 +21,15 @@ def kvc():
 class BothBook:
     """Library (all blocks) + oracle (block 0 only), compared as they go."""
 
-    def __init__(self, kvc, w):
+    def __init__(self, kvc, w, cross_frame_special=True, camera_only=False):
         self.kvc, self.w = kvc, w
+        self.policy = dict(cross_frame_special=cross_frame_special, camera_only=camera_only)
         self.lib = kvc.PagedKVCache(w.num_layers, w.num_heads, w.head_dim, w.page_size, w.dtype,
                                     w.scale_frames, w.sliding_window, w.headroom,
-                                    w.max_total_frames, device=None)
+                                    w.max_total_frames, device=None, **self.policy)
         self.orc = OraclePagedKV(1, w.page_size, w.num_heads, w.head_dim, w.dtype, w.scale_frames,
-                                 w.sliding_window, w.headroom, w.max_total_frames, mirror_blocks=())
+                                 w.sliding_window, w.headroom, w.max_total_frames, mirror_blocks=(),
+                                 **self.policy)
         bits = np.uint32 if w.dtype == "f32" else np.uint16
         self.dummy = np.zeros((w.tokens_per_frame, w.num_heads, w.head_dim), bits)
         self.plans = 0
@@ -38,9 +40,12 @@ class BothBook:
             self.orc.append_frame(0, self.dummy, self.dummy)
 
     def evict(self, b):
-        self.lib.evict_frames(b)
+        if self.policy["cross_frame_special"] and not self.policy["camera_only"]:
+            self.lib.evict_frames(b)
+        else:
+            self.lib.evict_frames(b, **self.policy)       # kvc_evict_frames_ex
         if b == 0:
-            self.orc.evict_frames(0, self.w.scale_frames, self.w.sliding_window)
+            self.orc.evict_frames(0, self.w.scale_frames, self.w.sliding_window, **self.policy)
 
     def set_defer(self, on):
         self.lib.set_defer_eviction(on)
@@ -65,6 +70,7 @@ class BothBook:
         idx, indptr, lpl = self.lib.plan_table()
         o_idx, o_indptr, o_lpl, _ = self.orc.visible_page_table(0)
         assert (idx, indptr, lpl) == (o_idx, o_indptr, o_lpl)
+        assert tuple(self.lib.plan_ranges()) == tuple(self.orc.visible_ranges(0))
         self.plans += 1
 
     def attend(self, b, f):
@@ -151,3 +157,35 @@ def test_plan_and_run_preconditions(kvc):
     with pytest.raises(kvc.KvcError) as e:
         lib.append_frame(0)
     assert e.value.code == "SPECIAL_POOL_FULL"
+
+
+@pytest.mark.parametrize("cross,cam", [(False, False), (True, True)])
+@pytest.mark.parametrize("name", ["tiny", "defer", "s518", "win518"])
+def test_special_policy_plans_match_oracle_every_frame(kvc, name, cross, cam):
+    """The special-token policies (cross_frame_special off; camera_only):
+    visible row ranges, deques and stats equal the oracle's at every frame,
+    through deferral, rollback and window resets."""
+    w = WORKLOADS[name]
+    if name == "win518":
+        w = w.with_(n_frames=w.window_frames + 40)
+    e = BothBook(kvc, w.with_(num_layers=min(w.num_layers, 2)), cross_frame_special=cross, camera_only=cam)
+    drive(w.with_(num_layers=min(w.num_layers, 2)), e)
+    assert e.plans > 0
+    e.lib.close()
+
+
+def test_special_policy_evict_arguments_must_match(kvc):
+    c = kvc.PagedKVCache(1, 2, 32, 16, "f32", 2, 4, 2, 16, device=None, cross_frame_special=False)
+    c.append_frame(0)
+    c.evict_frames(0, cross_frame_special=False, camera_only=False)
+    for kw in ({"cross_frame_special": True}, {"camera_only": True}):
+        with pytest.raises(kvc.KvcError) as e:
+            c.evict_frames(0, **kw)
+        assert e.value.code == "INVALID_ARG"
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_required_bytes(kvc.make_config(1, 2, 32, 16, "f32").__class__(
+            *[getattr(kvc.make_config(1, 2, 32, 16, "f32"), f) for f, _ in kvc.kvc_config._fields_[:-1]], 7))
+    g = kvc.kvc_get_geometry(kvc.make_config(1, 16, 64, 999, camera_only=True))
+    assert (g.num_camera_pages, g.max_num_pages) == (3, 88 + 13 + 3)
+    assert kvc.kvc_get_geometry(kvc.make_config(1, 16, 64, 999)).num_camera_pages == 0
+    c.close()
