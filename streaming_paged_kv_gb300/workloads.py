@@ -75,7 +75,16 @@ WORKLOADS = {
     # 518x378 windowed: 128 slots = 8 scale + 120 keyframe slots, keyframe every 13 frames.
     "win518": Workload(5, "win518", 24, 16, 64, "bf16", 999, 8, 120, 16, 2048, 25000,
                        mode="windowed", keyframe_interval=13, window_slots=128),
+    # The camera head's own cache beside the trunk's ([SLOTS] "特殊 token 流", last
+    # sentence: the camera head keeps an isomorphic, independent KV cache with the
+    # same scale / window parameters).  The pages give no shapes; reading: the same
+    # per-frame token layout and width as the 518x378 trunk, 4 layers of its own,
+    # K scaled per head like the trunk's.  Driven frame by frame with "s518".
+    "cam518": Workload(6, "cam518", 4, 16, 64, "bf16", 999, 8, 64, 16, 2048, 2048, k_head_scale=True),
 }
+
+# Streams made of two caches driven in lockstep: (trunk, camera head).
+PAIRED = {"camcache": ("s518", "cam518")}
 
 
 def schedule(w, decisions=None):
