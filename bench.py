@@ -33,7 +33,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "streamed frames/s (24-layer paged attn, 518x378); attn TFLOP/s vs GB300 roofline"
+STREAM_METRIC = "streamed frames/s ({layers}-layer paged attn, {label}); attention vs GB300 roofline"
 UNIT = "frames/s"
+LABELS = {"s518": "518x378 exact-page stream", "s224": "224x224 stream",
+          "defer": "224x224 keyframe + deferred-eviction stream", "win518": "518x378 windowed stream",
+          "tiny": "tiny fp32 stream"}
 
 
 def parse():
@@ -43,15 +47,18 @@ def parse():
     p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="s518",
-                   help="s518 (default, the streamed metric), s224, phase1, batch224 or win518")
+                   help="s518 (default, the streamed metric), s224, phase1, batch224, win518 or camcache")
     p.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     p.add_argument("--splits", type=int, default=0, help="tuning: force the KV split count (0 = the library's choice)")
+    p.add_argument("--qtiles", type=int, default=0,
+                   help="tuning: 128-row query tiles per CTA of the tensor-core kernel (0 = the library's choice)")
     p.add_argument("--pool", type=int, default=4, help="distinct input frames per layer")
     p.add_argument("--batch", type=int, default=8, help="streams of --workload batch224")
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--e2e-steps", type=int, default=64)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the compact lines of the other workloads after the default measurement")
     p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work")
     p.add_argument("--layers", type=int, default=None,
                    help="profiling size only: override the number of layers")
@@ -60,15 +67,73 @@ def parse():
     return p.parse_args()
 
 
+_PEAKS = None
+
+
 def peaks():
+    """Roofline denominators: the measured copy bandwidth and bf16 GEMM rates
+    of this GPU model (MEASURED_PEAKS.json), else one earlier GB300
+    measurement, with a warning on stderr."""
+    global _PEAKS
+    if _PEAKS is not None:
+        return _PEAKS
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         d = json.load(open(path))
-        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+        _PEAKS = {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                  "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
     except Exception:
-        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-                "source": "fallback"}
+        sys.stderr.write("bench.py: MEASURED_PEAKS.json not found or unreadable; the roofline fractions "
+                         "use fallback peaks (6800 GB/s, 1900 / 1700 TFLOP/s bf16 burst / sustained)\n")
+        _PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+    return _PEAKS
+
+
+def roof_bound(flops, bytes_alg):
+    """'tensor' when the arithmetic intensity is at or above the ridge point of
+    the burst bf16 peak over the copy bandwidth, else 'hbm'."""
+    pk = peaks()
+    return "tensor" if flops / max(bytes_alg, 1.0) >= pk["bf16_tflops"] * 1e3 / pk["hbm_gbs"] else "hbm"
+
+
+def attn_roofline(bound, flops, bytes_alg, attn_ms, attn_launches, step_ms, kernel, traffic=None):
+    """Roofline of the attention launches of a timed region.
+
+    achieved = algorithmic work (flops = 4 n_q N_kv H D, or bytes = visible K/V
+    once + Q in + O out) / the launches' CUDA-event time; `frac` divides by
+    the burst bf16 peak (a tensor-bound launch is a fraction of a second) or
+    the copy bandwidth.  `frac_sustained` is the same against the sustained
+    bf16 peak, and `step_frac` is the roofline time of all timed launches
+    (max of flops / peak and bytes / bandwidth) over the whole timed region,
+    so that everything outside the attention launches counts against it."""
+    pk = peaks()
+    n = max(attn_launches, 1)
+    secs = attn_ms / 1e3
+    tflops = flops / secs / 1e12 if attn_ms > 0 else None
+    gbs = bytes_alg / secs / 1e9 if attn_ms > 0 else None
+    roof_s = max(flops / (pk["bf16_tflops"] * 1e12), bytes_alg / (pk["hbm_gbs"] * 1e9))
+    r = {"bound": bound}
+    if bound == "tensor":
+        r.update({"achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                  "frac": tflops / pk["bf16_tflops"] if tflops else None})
+    else:
+        r.update({"achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                  "frac": gbs / pk["hbm_gbs"] if gbs else None})
+    r["traffic"] = traffic
+    r["peak_kind"] = (f"bf16 dense burst ({pk['source']})" if bound == "tensor"
+                      else f"HBM copy bandwidth ({pk['source']})")
+    r["frac_sustained"] = tflops / pk["bf16_tflops_sustained"] if (tflops and bound == "tensor") else None
+    r["peak_sustained"] = pk["bf16_tflops_sustained"] if bound == "tensor" else None
+    r["step_frac"] = roof_s / (step_ms / 1e3) if step_ms > 0 else None
+    r["attn_tflops"] = tflops
+    r["attn_gbs"] = gbs
+    r["kernel"] = kernel
+    r["flops_per_launch"] = flops / n
+    r["alg_bytes_per_launch"] = bytes_alg / n
+    r["launch_ms"] = attn_ms / n
+    r["outside_attn_ms_per_step"] = None
+    return r
 
 
 # ------------------------------------------------------------------ clocks
@@ -124,7 +189,7 @@ class ClockSampler:
 class Stream:
     """One device stream of the workload through the library."""
 
-    def __init__(self, kvc, w, pool, seed, kernel, dev, splits=0):
+    def __init__(self, kvc, w, pool, seed, kernel, dev, splits=0, qtiles=0):
         import torch
         from streaming_paged_kv_gb300.inputs import k_head_scale
         self.torch, self.kvc, self.w = torch, kvc, w
@@ -135,6 +200,8 @@ class Stream:
             self.c.set_option(kvc.KVC_OPT_ATTN_KERNEL, kernel)
         if splits:
             self.c.set_option(kvc.KVC_OPT_NUM_SPLITS, splits)
+        if qtiles:
+            self.c.set_option(kvc.KVC_OPT_QUERY_TILES, qtiles)
         T, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
@@ -251,7 +318,7 @@ def run_ours(args, rank, world):
     W = args.warmup
     K = max(1, min(K, w.n_frames))
     W = max(0, min(W, w.n_frames - K))
-    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits)
+    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits, args.qtiles)
     st.fast_forward(w.n_frames - K - W)
     for _ in range(W):
         st.step()
@@ -300,40 +367,127 @@ def run_ours(args, rank, world):
     if status != 0:
         raise RuntimeError(f"device status {status}")
     value = total_frames / (ms / 1e3)
-    pk = peaks()
-    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
-    roofline = {
-        "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
-        "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None,
-        "traffic": profiled_traffic(bytes_alg / max(attn_launches, 1)),
-        "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
-        "kernel": "paged attention (kvc_run attention launch)",
-        "flops_per_launch": flops / max(attn_launches, 1),
-        "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
-        "launch_ms": attn_ms / max(attn_launches, 1),
-        "hbm_frac_alg": (bytes_alg / (attn_ms / 1e3) / 1e9) / pk["hbm_gbs"] if attn_ms > 0 else None,
-    }
+    bound = roof_bound(flops, bytes_alg)
+    roofline = attn_roofline(bound, flops, bytes_alg, attn_ms, attn_launches, ms,
+                             "paged attention (kvc_run attention launch)",
+                             profiled_traffic(bytes_alg / max(attn_launches, 1)) if w.name == "s518" else None)
+    roofline["outside_attn_ms_per_step"] = (ms - attn_ms) / K
     res = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "metric": METRIC if w.name == "s518" else STREAM_METRIC.format(label=LABELS.get(w.name, w.name),
+                                                                        layers=w.num_layers),
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: 518x378 exact-page stream, {w.num_layers} layers, "
+        "config": {"workload": f"{w.name}: {LABELS.get(w.name, w.name)}, {w.num_layers} layers, "
                                f"H={H}, D={D}, page_size={w.page_size}, {w.n_frames} frames; timed = "
                                f"last {K} frames",
                    "frames_timed": [w.n_frames - K, w.n_frames - 1],
-                   "l2": "no flush: every layer's visible K/V (>300 MB at full context) exceeds L2",
+                   "l2": ("no flush: every layer's visible K/V (>300 MB at full context) exceeds L2"
+                          if w.name == "s518" else
+                          "no flush: the 24 layers' visible K/V together exceed L2, and each layer is "
+                          "read once per frame"),
                    "parallelism": f"replicas x{world} (independent streams, no collective)",
                    "wall_s": t_wall},
         "roofline": roofline,
-        "attn_tflops": achieved,
+        "attn_tflops": roofline["attn_tflops"],
         "gpu_launches": launches,
         "clocks": clk,
     }
     del st
     torch.cuda.empty_cache()
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, kvc, w, dev, rank, world)
+        res["e2e"] = run_e2e(args, kvc, w, dev, rank, world, K, W)
     return res
+
+
+PAIRED_METRIC = ("streamed frames/s (518x378: 24-layer trunk + 4-layer camera-head paged attn, two caches); "
+                 "attn TFLOP/s vs GB300 roofline")
+
+
+def run_paired(args, rank, world):
+    """The trunk's cache and the camera head's own cache in one stream: per
+    frame every trunk layer appends, evicts, plans (layer 0) and attends, then
+    every camera-head layer does the same on its cache.  Timed: the last K
+    frames of the 2048-frame stream, as for the trunk alone."""
+    import torch
+    from streaming_paged_kv_gb300 import build
+    build.build()
+    from streaming_paged_kv_gb300 import kvc
+    from streaming_paged_kv_gb300.workloads import PAIRED, WORKLOADS
+    tw, hw = (WORKLOADS[n] for n in PAIRED["camcache"])
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    K = args.steps if args.steps is not None else 20
+    W = max(args.warmup, 3)
+    streams = [Stream(kvc, w, args.pool, args.seed + rank + 17 * i, args.kernel, dev, args.splits, args.qtiles)
+               for i, w in enumerate((tw, hw))]
+    for st in streams:
+        st.fast_forward(tw.n_frames - K - W)
+    for _ in range(W):
+        for st in streams:
+            st.step()
+    torch.cuda.synchronize()
+    n_q, H, D = tw.tokens_per_frame, tw.num_heads, tw.head_dim
+    book = kvc.PagedKVCache(1, H, D, tw.page_size, tw.dtype, tw.scale_frames, tw.sliding_window,
+                            tw.headroom, tw.max_total_frames, device=None)
+    flops = bytes_alg = 0.0
+    layers = tw.num_layers + hw.num_layers
+    for f in range(tw.n_frames):
+        book.append_frame(0)
+        book.evict_frames(0)
+        if f >= tw.n_frames - K:
+            s_ = book.stats(0)
+            nkv = tw.page_size * (s_["scale_pages"] + s_["live_pages"]) + s_["special_tokens"]
+            flops += layers * 4.0 * n_q * nkv * H * D
+            bytes_alg += layers * (2.0 * nkv * H * D * 2 + 2.0 * n_q * H * D * 2)
+    book.close()
+    for st in streams:
+        kvc.kvc_get_counters(st.c.h, reset=True)
+        st.c.set_option(kvc.KVC_OPT_TIMING, 1)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(K):
+        for st in streams:
+            st.step()
+    ev1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms, total_frames = aggregate(ev0.elapsed_time(ev1), K, world, dev)
+    launches = attn_launches = 0
+    attn_ms = 0.0
+    for st in streams:
+        l_, a_, m_ = kvc.kvc_get_counters(st.c.h, reset=True)
+        launches, attn_launches, attn_ms = launches + l_, attn_launches + a_, attn_ms + m_
+        st.c.set_option(kvc.KVC_OPT_TIMING, 0)
+        if kvc.kvc_device_status(st.c.h, st.c._stream()) != 0:
+            raise RuntimeError("device status")
+    roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
+                         "paged attention (kvc_run attention launch, both caches)")
+    roof["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    del streams
+    torch.cuda.empty_cache()
+    return {
+        "metric": PAIRED_METRIC, "value": total_frames / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"camcache: {tw.name} trunk ({tw.num_layers} layers) + {hw.name} camera head "
+                               f"({hw.num_layers} layers), H={H}, D={D}, page_size={tw.page_size}; timed = last "
+                               f"{K} frames of {tw.n_frames}",
+                   "l2": "no flush: every layer's visible K/V exceeds L2",
+                   "parallelism": f"replicas x{world} (independent streams, no collective)"},
+        "roofline": roof, "attn_tflops": roof["attn_tflops"], "gpu_launches": launches, "clocks": clk,
+    }
 
 
 WINDOW_METRIC = ("windowed-stream frames/s (518x378, 24-layer paged attn, 128-slot window reset per window, "
@@ -359,7 +513,7 @@ def run_windowed(args, rank, world):
     torch.cuda.set_device(dev)
     K = min(args.steps or w.window_frames, w.window_frames)
     W = max(args.warmup, 3)
-    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits)
+    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits, args.qtiles)
     c, L = st.c, w.num_layers
     book = kvc.PagedKVCache(1, w.num_heads, w.head_dim, w.page_size, w.dtype, w.scale_frames,
                             w.sliding_window, w.headroom, w.max_total_frames, device=None)
@@ -439,8 +593,10 @@ def run_windowed(args, rank, world):
     T, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
     flops = sum(L * 4.0 * T * n * H * D for n in nkv)
     bytes_alg = sum(L * (2.0 * n * H * D * 2 + 2.0 * T * H * D * 2) for n in nkv)
-    pk = peaks()
-    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
+    roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
+                         "paged attention (kvc_run attention launch)")
+    roof["outside_attn_ms_per_step"] = (ms - attn_ms) / max(n_frames, 1)
+    achieved = roof["attn_tflops"]
     book.close()
     del st
     torch.cuda.empty_cache()
@@ -455,14 +611,7 @@ def run_windowed(args, rank, world):
                    "parallelism": f"replicas x{world} (independent streams, no collective)"},
         "frame_ms": {"p50": per[len(per) // 2], "p99": per[min(len(per) - 1, int(len(per) * 0.99))],
                      "max": per[-1]},
-        "roofline": {
-            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None, "traffic": None,
-            "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
-            "kernel": "paged attention (kvc_run attention launch)",
-            "flops_per_launch": flops / max(attn_launches, 1),
-            "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
-            "launch_ms": attn_ms / max(attn_launches, 1)},
+        "roofline": roof,
         "attn_tflops": achieved,
         "gpu_launches": launches,
         "clocks": clk,
@@ -538,8 +687,10 @@ def run_phase1(args, rank, world):
         raise RuntimeError("device status")
     flops = K * L * 4.0 * n_q * n_q * H * D
     bytes_alg = K * L * (2.0 * n_q * H * D * 2 + 2.0 * n_q * H * D * 2)
-    pk = peaks()
-    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
+    roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
+                         "paged attention (kvc_run attention launch inside kvc_prefill)")
+    roof["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    achieved = roof["attn_tflops"]
     c.close()
     return {
         "metric": PHASE1_METRIC, "value": total_steps * F / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
@@ -549,14 +700,7 @@ def run_phase1(args, rank, world):
                                f"page_size={w.page_size}; one step = clean + prefill of every layer",
                    "l2": "no flush: the layers' caches (33 MB of K/V each, 24 blocks) exceed L2 together",
                    "parallelism": f"replicas x{world} (independent streams, no collective)"},
-        "roofline": {
-            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None, "traffic": None,
-            "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
-            "kernel": "paged attention (kvc_run attention launch inside kvc_prefill)",
-            "flops_per_launch": flops / max(attn_launches, 1),
-            "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
-            "launch_ms": attn_ms / max(attn_launches, 1)},
+        "roofline": roof,
         "attn_tflops": achieved,
         "gpu_launches": launches,
         "clocks": clk,
@@ -586,7 +730,8 @@ def run_batch224(args, rank, world):
     K = args.steps if args.steps is not None else 60
     W = max(args.warmup, 3)
     start = w.n_frames - K - W        # the timed frames are the stream's last K
-    streams = [Stream(kvc, w, args.pool, args.seed + rank * 64 + i, args.kernel, dev) for i in range(B)]
+    streams = [Stream(kvc, w, args.pool, args.seed + rank * 64 + i, args.kernel, dev, args.splits, args.qtiles)
+               for i in range(B)]
     for st in streams:
         st.fast_forward(start)
     T, H, D, L = w.tokens_per_frame, w.num_heads, w.head_dim, w.num_layers
@@ -641,8 +786,10 @@ def run_batch224(args, rank, world):
     for st in streams:
         if kvc.kvc_device_status(st.c.h, st.c._stream()) != 0:
             raise RuntimeError("device status")
-    pk = peaks()
-    achieved = flops / (attn_ms / 1e3) / 1e12 if attn_ms > 0 else None
+    roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
+                         "paged attention (one kvc_run_batch launch per layer)")
+    roof["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    achieved = roof["attn_tflops"]
     res = {
         "metric": BATCH_METRIC, "value": total_steps * B / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
@@ -652,14 +799,7 @@ def run_batch224(args, rank, world):
                                f"stream ({nkv} visible tokens)",
                    "l2": "no flush: the streams' visible K/V per layer together exceed L2",
                    "parallelism": f"replicas x{world} (independent streams, no collective)"},
-        "roofline": {
-            "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": achieved / pk["bf16_tflops_sustained"] if achieved else None, "traffic": None,
-            "peak_kind": f"bf16 sustained ({pk['source']}); burst {pk['bf16_tflops']}",
-            "kernel": "paged attention (one kvc_run_batch launch per layer)",
-            "flops_per_launch": flops / max(attn_launches, 1),
-            "alg_bytes_per_launch": bytes_alg / max(attn_launches, 1),
-            "launch_ms": attn_ms / max(attn_launches, 1)},
+        "roofline": roof,
         "attn_tflops": achieved,
         "gpu_launches": launches,
         "clocks": clk,
@@ -669,14 +809,15 @@ def run_batch224(args, rank, world):
     return res
 
 
-def run_e2e(args, kvc, w, dev, rank, world):
-    """The same frames/s through the public API with host inputs: every step
-    copies that frame's Q/K/V of every layer from pinned host memory and reads
-    every layer's output back to pinned host memory inside the timed region
-    (on their own streams, overlapping the attention launches)."""
+def run_e2e(args, kvc, w, dev, rank, world, K, W):
+    """The same frames/s through the public API with host inputs, over the
+    same frames of the stream as the device-timed number: every step copies
+    that frame's Q/K/V of every layer from pinned host memory and reads every
+    layer's output back to pinned host memory inside the timed region (on
+    their own streams, overlapping the attention launches)."""
     import torch
-    K = max(1, min(args.e2e_steps, w.n_frames))
-    W = min(4, w.n_frames - K)
+    K = max(1, min(K, w.n_frames))
+    W = max(0, min(W, w.n_frames - K))
     T, H, D, L = w.tokens_per_frame, w.num_heads, w.head_dim, w.num_layers
     c = kvc.PagedKVCache(L, H, D, w.page_size, w.dtype, w.scale_frames, w.sliding_window,
                          w.headroom, w.max_total_frames, device=dev)
@@ -739,6 +880,42 @@ def run_e2e(args, kvc, w, dev, rank, world):
     return {"value": total_frames / dt, "unit": UNIT, "h2d_bytes_per_step": L * 3 * T * H * D * 2,
             "d2h_bytes_per_step": L * T * H * D * 2, "steps": K,
             "frames_timed": [w.n_frames - K, w.n_frames - 1]}
+
+
+def compact(r):
+    """The headline fields of another workload's bench line."""
+    roof = r.get("roofline", {})
+    keep = ("bound", "achieved", "peak", "unit", "frac", "frac_sustained", "step_frac", "attn_tflops",
+            "launch_ms", "outside_attn_ms_per_step")
+    out = {"metric": r["metric"], "value": r["value"], "unit": r["unit"], "steps": r["steps"],
+           "ms_per_step": r["ms_per_step"], "workload": r["config"]["workload"],
+           "roofline": {k: roof.get(k) for k in keep}, "gpu_launches": r.get("gpu_launches"),
+           "clocks": r.get("clocks")}
+    if "frame_ms" in r:
+        out["frame_ms"] = r["frame_ms"]
+    return out
+
+
+def run_extra(args, rank, world):
+    """The other workloads' numbers, measured in the same run after the
+    default one: the windowed long stream (one whole window from its clean
+    start, with per-frame latency percentiles), the last 60 frames of the
+    224x224 stream, 8 batched 224x224 streams (one attention launch per
+    layer), and the trunk's cache beside the camera head's own cache."""
+    import torch
+    extra = {}
+    plans = (("win518", run_windowed, {"steps": None, "warmup": 5}),
+             ("s224", run_ours, {"workload": "s224", "steps": 60, "warmup": 5, "no_e2e": True}),
+             ("batch224", run_batch224, {"steps": 60, "warmup": 5}),
+             ("camcache", run_paired, {"steps": 20, "warmup": 5}))
+    for name, fn, over in plans:
+        a = argparse.Namespace(**vars(args))
+        a.layers = a.frames = None
+        for k, v in over.items():
+            setattr(a, k, v)
+        extra[name] = compact(fn(a, rank, world))
+        torch.cuda.empty_cache()
+    return extra
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -846,8 +1023,12 @@ def run_reference(args):
     cb = {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
           "sample": f"per step: {rows}/{n_q} query rows x {w.num_heads} heads of one layer of the last "
                     f"frame, scaled to a {w.num_layers}-layer frame, plus bookkeeping"}
+    # ms_per_step is what a step took (one sample); the whole-frame time is an
+    # extrapolation from it and is reported beside it.
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
-            "steps": K, "warmup": W, "ms_per_step": per_frame * 1e3, "higher_is_better": True,
+            "steps": K, "warmup": W, "ms_per_step": secs / K * 1e3,
+            "sample_s_per_step": secs / K, "extrapolated_ms_per_frame": per_frame * 1e3,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{w.name}: 518x378 exact-page stream, {w.num_layers} layers, "
                                    f"H={w.num_heads}, D={w.head_dim}, page_size={w.page_size}, "
@@ -869,8 +1050,9 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    if args.workload in ("phase1", "batch224", "win518"):
-        res = {"phase1": run_phase1, "batch224": run_batch224, "win518": run_windowed}[args.workload](args, rank, world)
+    if args.workload in ("phase1", "batch224", "win518", "camcache"):
+        res = {"phase1": run_phase1, "batch224": run_batch224, "win518": run_windowed,
+               "camcache": run_paired}[args.workload](args, rank, world)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if world > 1:
@@ -879,6 +1061,8 @@ def main():
             torch.distributed.destroy_process_group()
         return 0
     res = run_ours(args, rank, world)
+    if args.workload == "s518" and not args.no_extra and not (args.layers or args.frames):
+        res["extra"] = run_extra(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(workload(args), args.seed, args.cpu_budget)
