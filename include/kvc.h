@@ -299,9 +299,10 @@ enum {
   KVC_OPT_STALL_TEST = 5,  /* test only, 1: the tensor-core kernel first waits on a barrier
                               that nothing signals, so its bounded wait runs out and the run
                               reports KVC_ERR_DEVICE_TIMEOUT (no output is written)           */
-  KVC_OPT_QUERY_TILES = 6  /* tensor-core kernel: 128-row query tiles per CTA; 0 auto,
-                              1 (both softmax warp groups share one tile, taking alternate
-                              KV tiles), 2 (one warp group per tile)                         */
+  KVC_OPT_QUERY_TILES = 6  /* tensor-core kernel: 128-row query tiles per CTA; 0 auto (a
+                              cost model picks tiles and splits per launch), 1 (both softmax
+                              warp groups share one tile, taking alternate KV tiles), 2 (one
+                              warp group per tile)                                           */
 };
 int kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
 

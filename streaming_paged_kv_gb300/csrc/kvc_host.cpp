@@ -221,23 +221,65 @@ int attn_kernel_for(const kvc_handle* h) {
   return tc ? 2 : 1;
 }
 
-// Query tiles (128 rows) per CTA of the tensor-core kernel.
-int q_tiles_for(const kvc_handle* h) { return h->opt_qtiles > 0 ? h->opt_qtiles : 2; }
+// Launch shape of an attention launch: 128-row query tiles per CTA of the
+// tensor-core kernel and the number of KV splits.
+struct Shape {
+  int qt, splits;
+};
+
+// Cost model of the tensor-core kernel in microseconds, fitted to GB300
+// measurements at 518x378 full context (one CTA per SM; CTAs run in waves):
+// a CTA costs fixed + tiles * per_tile, with per_tile 0.985 us and fixed
+// 6.2 us for two query tiles per CTA, 0.522 us and 4.9 us for one (both
+// softmax groups on it); the merge reads splits * rows * H * (D + 1) fp32 at
+// about 5 TB/s after a 2 us launch.  base_ctas(qt) = CTAs of one split.
+double tc_cost_us(int qt, int s, int64_t base_ctas, int64_t max_tiles, int64_t merge_elems, int num_sms) {
+  const double per_tile = qt == 2 ? 0.985 : 0.522, fixed = qt == 2 ? 6.2 : 4.9;
+  const int64_t sms = num_sms > 0 ? num_sms : 1;
+  const int64_t waves = (base_ctas * s + sms - 1) / sms;
+  const double cta = fixed + per_tile * (double)((max_tiles + s - 1) / s);
+  const double merge = s > 1 ? 2.0 + (double)s * (double)merge_elems * 4.0 / 5.0e6 : 0.0;
+  return (double)waves * cta + merge;
+}
+
+// Best shape over qt in {2, 1} and splits in [1, max_s]; one tile per CTA
+// must win by 3% (the model is a fit).  rows_blocks(qt) = sum over requests of
+// ceil(n_q / (128 qt)).  Options force either choice.
+Shape choose_tc_shape(const kvc_handle* h, int max_s, int64_t blocks2, int64_t blocks1, int64_t max_tiles,
+                      int64_t rows_total) {
+  const int64_t H = h->cfg.num_heads;
+  const int64_t merge_elems = rows_total * H * (h->cfg.head_dim + 1);
+  Shape best{2, 1};
+  double best_cost = 1e300;
+  for (int qt = 2; qt >= 1; --qt) {
+    if (h->opt_qtiles > 0 && qt != h->opt_qtiles) continue;
+    const int64_t base = (qt == 2 ? blocks2 : blocks1) * H;
+    for (int sp = 1; sp <= max_s; ++sp) {
+      if (h->opt_splits > 0 && sp != (h->opt_splits < max_s ? h->opt_splits : max_s)) continue;
+      double c = tc_cost_us(qt, sp, base, max_tiles, merge_elems, h->num_sms);
+      if (qt == 1) c *= 1.03;
+      if (c < best_cost - 1e-9) { best_cost = c; best = Shape{qt, sp}; }
+    }
+  }
+  return best;
+}
 
 int tile_rows_for(const kvc_handle* h, int kernel) {
   return kernel == 2 ? kvc::kTcTileRows : kvc::simt_tile_rows(h->cfg.head_dim);
 }
 
-// Number of KV splits: balance waves of CTAs against work per split, with a
-// small charge per split for the merge.
-int choose_splits(const kvc_handle* h, int kernel, int32_t n_q) {
+// Launch shape of one request.  Tensor-core kernel: the cost model above.
+// CUDA-core kernel (128-row query blocks, two CTAs per SM): balance waves of
+// CTAs against work per split, with a small charge per split for the merge.
+Shape choose_shape(const kvc_handle* h, int kernel, int32_t n_q) {
   int max_s = h->cfg.max_kv_splits;
   if (max_s > h->plan_n_tiles) max_s = h->plan_n_tiles;
   if (max_s < 1) max_s = 1;
-  if (h->opt_splits > 0) return h->opt_splits < max_s ? h->opt_splits : max_s;
-  int q_rows = kernel == 2 ? 128 * q_tiles_for(h) : 128;
-  int64_t base = (int64_t)((n_q + q_rows - 1) / q_rows) * h->cfg.num_heads;
-  int64_t slots = (int64_t)h->num_sms * (kernel == 2 ? 1 : 2);
+  if (kernel == 2)
+    return choose_tc_shape(h, max_s, (n_q + 255) / 256, (n_q + 127) / 128, h->plan_n_tiles, n_q);
+  if (h->opt_splits > 0) return Shape{1, h->opt_splits < max_s ? h->opt_splits : max_s};
+  int64_t base = (int64_t)((n_q + 127) / 128) * h->cfg.num_heads;
+  int64_t slots = (int64_t)h->num_sms * 2;
   double best = 1e300;
   int best_s = 1;
   for (int s = 1; s <= max_s; ++s) {
@@ -246,7 +288,7 @@ int choose_splits(const kvc_handle* h, int kernel, int32_t n_q) {
     double cost = (double)waves * per * (1.0 + (s > 1 ? 0.02 * s : 0.0));
     if (cost < best - 1e-9) { best = cost; best_s = s; }
   }
-  return best_s;
+  return Shape{1, best_s};
 }
 
 void record_timing(kvc_handle* h, int which, cudaStream_t st) {
@@ -332,7 +374,7 @@ kvc::TcBatchArgs tc_batch_header(const kvc_handle* h, const void* Q, void* out, 
   tb.dtype = h->cfg.dtype;
   tb.stall_test = h->stall_test;
   tb.num_sms = h->num_sms;
-  tb.q_tiles = q_tiles_for(h);
+  tb.q_tiles = 2;
   tb.sm_scale_log2 = h->cfg.sm_scale * 1.4426950408889634f;
   tb.wait_budget = h->wait_budget > 0 ? h->wait_budget : 4000000000LL;
   return tb;
@@ -644,13 +686,15 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
   int rc = check_run(h, block, Q, out, n_q);
   if (rc || n_q == 0) return rc;
   const int kernel = h->plan_kernel;
-  const int splits = choose_splits(h, kernel, n_q);
+  const Shape shape = choose_shape(h, kernel, n_q);
+  const int splits = shape.splits;
   const kvc::AttnArgs a = attn_args(h, block, Q, out, n_q, splits);
   cudaStream_t st = (cudaStream_t)stream;
   if (h->timing) record_timing(h, 0, st);
   cudaError_t err;
   if (kernel == 2) {
     kvc::TcBatchArgs tb = tc_batch_header(h, Q, out, n_q);
+    tb.q_tiles = shape.qt;
     tb.count = 1;
     tb.req[0] = tc_request(h, block, 0, n_q, splits);
     err = kvc::launch_attn_tc(tb, st);
@@ -713,34 +757,25 @@ int kvc_run_batch(kvc_handle* const* hs, const int32_t* blocks, int32_t count, c
     }
     return KVC_OK;
   }
-  // One split count for the whole launch: balance waves of all requests'
-  // CTAs against the largest per-split tile count.
+  // One shape for the whole launch: the cost model over all requests' CTAs,
+  // the largest per-request tile count and all requests' merge traffic.
   kvc_handle* h0 = hs[0];
   int max_s = 1 << 30, max_tiles = 1;
-  int64_t base = 0;
+  int64_t blocks2 = 0, blocks1 = 0;
   for (int32_t r = 0; r < count; ++r) {
     const kvc_handle* h = hs[r];
     const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
     if (h->cfg.max_kv_splits < max_s) max_s = h->cfg.max_kv_splits;
     if (h->plan_n_tiles > max_tiles) max_tiles = h->plan_n_tiles;
-    const int q_rows = 128 * q_tiles_for(h0);
-    base += (int64_t)((n_q + q_rows - 1) / q_rows) * h->cfg.num_heads;
+    blocks2 += (n_q + 255) / 256;
+    blocks1 += (n_q + 127) / 128;
   }
+  if (max_s > max_tiles) max_s = max_tiles;
   if (max_s < 1) max_s = 1;
-  int splits = 1;
-  if (h0->opt_splits > 0) {
-    splits = h0->opt_splits < max_s ? h0->opt_splits : max_s;
-  } else {
-    const int64_t slots = h0->num_sms;
-    double best = 1e300;
-    for (int s = 1; s <= max_s; ++s) {
-      const int64_t waves = (base * s + slots - 1) / slots;
-      const int64_t per = (max_tiles + s - 1) / s;
-      const double cost = (double)waves * per * (1.0 + (s > 1 ? 0.02 * s : 0.0));
-      if (cost < best - 1e-9) { best = cost; splits = s; }
-    }
-  }
+  const Shape shape = choose_tc_shape(h0, max_s, blocks2, blocks1, max_tiles, rows);
+  const int splits = shape.splits;
   kvc::TcBatchArgs tb = tc_batch_header(h0, Q, out, rows);
+  tb.q_tiles = shape.qt;
   tb.count = count;
   for (int32_t r = 0; r < count; ++r) {
     const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
