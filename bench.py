@@ -372,6 +372,7 @@ def run_ours(args, rank, world):
                              "paged attention (kvc_run attention launch)",
                              profiled_traffic(bytes_alg / max(attn_launches, 1)) if w.name == "s518" else None)
     roofline["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    roofline["launch_shape"] = dict(zip(("q_tiles", "splits"), kvc.kvc_get_launch_shape(st.c.h)))
     res = {
         "metric": METRIC if w.name == "s518" else STREAM_METRIC.format(label=LABELS.get(w.name, w.name),
                                                                         layers=w.num_layers),
@@ -475,6 +476,7 @@ def run_paired(args, rank, world):
     roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
                          "paged attention (kvc_run attention launch, both caches)")
     roof["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    roof["launch_shape"] = dict(zip(("q_tiles", "splits"), kvc.kvc_get_launch_shape(streams[0].c.h)))
     del streams
     torch.cuda.empty_cache()
     return {
@@ -596,6 +598,7 @@ def run_windowed(args, rank, world):
     roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
                          "paged attention (kvc_run attention launch)")
     roof["outside_attn_ms_per_step"] = (ms - attn_ms) / max(n_frames, 1)
+    roof["launch_shape"] = dict(zip(("q_tiles", "splits"), kvc.kvc_get_launch_shape(c.h)))
     achieved = roof["attn_tflops"]
     book.close()
     del st
@@ -690,6 +693,7 @@ def run_phase1(args, rank, world):
     roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
                          "paged attention (kvc_run attention launch inside kvc_prefill)")
     roof["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    roof["launch_shape"] = dict(zip(("q_tiles", "splits"), kvc.kvc_get_launch_shape(c.h)))
     achieved = roof["attn_tflops"]
     c.close()
     return {
@@ -789,6 +793,7 @@ def run_batch224(args, rank, world):
     roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
                          "paged attention (one kvc_run_batch launch per layer)")
     roof["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    roof["launch_shape"] = dict(zip(("q_tiles", "splits"), kvc.kvc_get_launch_shape(h0.h)))
     achieved = roof["attn_tflops"]
     res = {
         "metric": BATCH_METRIC, "value": total_steps * B / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
@@ -886,7 +891,7 @@ def compact(r):
     """The headline fields of another workload's bench line."""
     roof = r.get("roofline", {})
     keep = ("bound", "achieved", "peak", "unit", "frac", "frac_sustained", "step_frac", "attn_tflops",
-            "launch_ms", "outside_attn_ms_per_step")
+            "launch_ms", "outside_attn_ms_per_step", "launch_shape")
     out = {"metric": r["metric"], "value": r["value"], "unit": r["unit"], "steps": r["steps"],
            "ms_per_step": r["ms_per_step"], "workload": r["config"]["workload"],
            "roofline": {k: roof.get(k) for k in keep}, "gpu_launches": r.get("gpu_launches"),

@@ -341,6 +341,11 @@ int kvc_paged_attention_static(const void* cache_block, int32_t dtype, int32_t n
                                const int32_t* valid_lens, int32_t n_pages, const void* Q, void* out,
                                int32_t n_q, float sm_scale, kvc_stream stream);
 
+/* Shape of the handle's latest attention launch (kvc_run, or kvc_run_batch
+ * with this handle first): 128-row query tiles per CTA of the tensor-core
+ * kernel (0 for the CUDA-core kernel) and KV splits.  Diagnostics. */
+int kvc_get_launch_shape(const kvc_handle* h, int32_t* q_tiles, int32_t* splits);
+
 /* Static message for a status code. */
 const char* kvc_strerror(int code);
 

@@ -178,6 +178,7 @@ struct kvc_handle {
   int stall_test = 0;
   // Counters.
   int64_t launches = 0, attn_launches = 0;
+  int32_t last_qt = 0, last_splits = 0;   // shape of the latest attention launch (0: CUDA-core kernel)
   double attn_ms = 0.0;
   cudaEvent_t* ev = nullptr;        // [2 * kEventPairs] when timing
   bool* ev_used = nullptr;
@@ -696,10 +697,14 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
     kvc::TcBatchArgs tb = tc_batch_header(h, Q, out, n_q);
     tb.q_tiles = shape.qt;
     tb.count = 1;
+    h->last_qt = shape.qt;
+    h->last_splits = splits;
     tb.req[0] = tc_request(h, block, 0, n_q, splits);
     err = kvc::launch_attn_tc(tb, st);
   } else {
     err = kvc::launch_attn_simt(a, h->cfg.dtype, st);
+    h->last_qt = 0;
+    h->last_splits = splits;
   }
   if (h->timing) record_timing(h, 1, st);
   if (err != cudaSuccess) return KVC_ERR_CUDA;
@@ -777,6 +782,8 @@ int kvc_run_batch(kvc_handle* const* hs, const int32_t* blocks, int32_t count, c
   kvc::TcBatchArgs tb = tc_batch_header(h0, Q, out, rows);
   tb.q_tiles = shape.qt;
   tb.count = count;
+  h0->last_qt = shape.qt;
+  h0->last_splits = splits;
   for (int32_t r = 0; r < count; ++r) {
     const int32_t n_q = qo_indptr[r + 1] - qo_indptr[r];
     const int s_r = splits < hs[r]->plan_n_tiles ? splits : hs[r]->plan_n_tiles;
@@ -1012,6 +1019,13 @@ int kvc_get_counters(kvc_handle* h, int64_t* kernel_launches, int64_t* attn_laun
     h->attn_launches = 0;
     h->attn_ms = 0.0;
   }
+  return KVC_OK;
+}
+
+int kvc_get_launch_shape(const kvc_handle* h, int32_t* q_tiles, int32_t* splits) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (q_tiles) *q_tiles = h->last_qt;
+  if (splits) *splits = h->last_splits;
   return KVC_OK;
 }
 

@@ -106,6 +106,7 @@ _SIGS = {
     "kvc_set_option": [_P, _I32, _I64],
     "kvc_get_counters": [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                          ctypes.POINTER(ctypes.c_double), _I32],
+    "kvc_get_launch_shape": [_P, _PI32, _PI32],
     "kvc_paged_attention_static": [_P, _I32, _I32, _I32, _I32, _PI32, _PI32, _I32, _P, _P, _I32,
                                    ctypes.c_float, _P],
 }
@@ -302,6 +303,13 @@ def kvc_paged_attention_static(cache_ptr, dtype, num_heads, head_dim, page_size,
                                                  head_dim, page_size, ids, valid, n, q_ptr, out_ptr,
                                                  n_q, float(sm_scale), stream),
                   "kvc_paged_attention_static")
+
+
+def kvc_get_launch_shape(h):
+    """(query tiles per CTA, KV splits) of the handle's latest attention launch."""
+    qt, sp = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.kvc_get_launch_shape(h, ctypes.byref(qt), ctypes.byref(sp)), "kvc_get_launch_shape")
+    return qt.value, sp.value
 
 
 def kvc_strerror(rc):

@@ -89,12 +89,13 @@ def _run(kvc, pool, w, check, rows=None, seed=0):
         torch.cuda.synchronize()
         dev = to_bits(c.cache_view(0).cpu())
         assert np.array_equal(dev, orc.mirror[0])                 # every cache byte
+        shape = kvc.kvc_get_launch_shape(c.h)
     finally:
         c.close()
     assert len(results) == len(check), results
     worst = max(r[2] for r in results), max(r[3] for r in results)
     assert worst[0] <= 2e-2 and worst[1] <= 5e-3, results
-    return results
+    return results, shape
 
 
 def test_s518_full_stream_sampled_rows(kvc, pool):
@@ -102,7 +103,10 @@ def test_s518_full_stream_sampled_rows(kvc, pool):
     rng = np.random.default_rng(4)
     check = {0, 1, 7, 8, 9, 71, 72, 73, 165, 166, 167, 1000, 2047} | set(rng.integers(0, 2048, 4).tolist())
     rows = sorted(set(range(0, 1005, 16)) | {1004, 6, 5})
-    _run(kvc, pool, w, check, rows)
+    _, shape = _run(kvc, pool, w, check, rows)
+    # The launch-shape model keeps two query tiles per CTA at full context
+    # (1005 rows: 4 query blocks x 16 heads, many KV splits).
+    assert shape[0] == 2 and shape[1] > 1, shape
 
 
 def test_windowed_one_window_and_reset(kvc, pool):
@@ -122,7 +126,10 @@ def test_deferred_stream_full(kvc, pool):
 def test_s224_full_stream(kvc, pool):
     w = WORKLOADS["s224"]
     check = {0, 41, 42, 72, 73, 150, 199}
-    _run(kvc, pool, w, check)
+    _, shape = _run(kvc, pool, w, check)
+    # Under one wave of two-tile CTAs (262 rows: 2 blocks x 16 heads) the model
+    # takes one query tile per CTA.
+    assert shape[0] == 1, shape
 
 
 def test_bounded_wait_reports_timeout_and_recovers(kvc):
