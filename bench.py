@@ -906,13 +906,15 @@ def run_extra(args, rank, world):
     default one: the windowed long stream (one whole window from its clean
     start, with per-frame latency percentiles), the last 60 frames of the
     224x224 stream, 8 batched 224x224 streams (one attention launch per
-    layer), and the trunk's cache beside the camera head's own cache."""
+    layer), the trunk's cache beside the camera head's own cache, and the
+    Phase-1 prefill of the scale frames."""
     import torch
     extra = {}
     plans = (("win518", run_windowed, {"steps": None, "warmup": 5}),
              ("s224", run_ours, {"workload": "s224", "steps": 60, "warmup": 5, "no_e2e": True}),
              ("batch224", run_batch224, {"steps": 60, "warmup": 5}),
-             ("camcache", run_paired, {"steps": 20, "warmup": 5}))
+             ("camcache", run_paired, {"steps": 20, "warmup": 5}),
+             ("phase1", run_phase1, {"steps": 10, "warmup": 3}))
     for name, fn, over in plans:
         a = argparse.Namespace(**vars(args))
         a.layers = a.frames = None
