@@ -54,3 +54,36 @@ def test_bookkeeping_handle_refuses_device_calls(kvc):
     assert e.value.code == "NO_DEVICE"
     assert kvc.kvc_device_status(c.h) == -11
     assert kvc.kvc_strerror(-7).startswith("stale plan")
+
+
+def test_debug_print_every_n_frames():
+    """KVC_DEBUG=N prints every block's slot usage every N plans (one per
+    streamed frame), like the pages' LINGBOT_DEBUG_KV ([SLOTS] "动手验证")."""
+    import subprocess
+    import sys
+    code = ("from streaming_paged_kv_gb300 import kvc\n"
+            "c = kvc.PagedKVCache(2, 2, 32, 16, 'f32', 2, 4, 2, 16, device=None)\n"
+            "for f in range(8):\n"
+            "    for b in range(2):\n"
+            "        c.append_frame(b); c.evict_frames(b)\n"
+            "    c.plan()\n")
+    env = dict(os.environ, KVC_DEBUG="4", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[kvc]")]
+    assert lines == [
+        "[kvc] frame 4 block 0: scale_pg=2 live_pg=2 free_pg=4 special=24",
+        "[kvc] frame 4 block 1: scale_pg=2 live_pg=2 free_pg=4 special=24",
+        "[kvc] frame 8 block 0: scale_pg=2 live_pg=4 free_pg=2 special=48",
+        "[kvc] frame 8 block 1: scale_pg=2 live_pg=4 free_pg=2 special=48",
+    ], r.stderr
+
+
+def test_geometry_and_launch_shape_accessors(kvc):
+    g = kvc.kvc_get_geometry(kvc.make_config(24, 16, 64, 999))
+    assert (g.num_patch_pages, g.frames_per_special_page, g.num_special_pages, g.max_num_pages,
+            g.tokens_per_frame) == (88, 166, 13, 101, 1005)
+    assert g.block_bytes == 101 * g.page_bytes == 101 * 2 * 999 * 16 * 64 * 2
+    c = kvc.PagedKVCache(1, 2, 32, 16, "f32", 2, 4, 2, 16, device=None)
+    assert kvc.kvc_get_launch_shape(c.h) == (0, 0)      # no attention launched
+    c.close()
