@@ -159,7 +159,7 @@ def test_plan_and_run_preconditions(kvc):
     assert e.value.code == "SPECIAL_POOL_FULL"
 
 
-@pytest.mark.parametrize("cross,cam", [(False, False), (True, True)])
+@pytest.mark.parametrize("cross,cam", [(False, False), (True, True), (False, True)])
 @pytest.mark.parametrize("name", ["tiny", "defer", "s518", "win518"])
 def test_special_policy_plans_match_oracle_every_frame(kvc, name, cross, cam):
     """The special-token policies (cross_frame_special off; camera_only):
