@@ -920,7 +920,12 @@ def run_extra(args, rank, world):
         a.layers = a.frames = None
         for k, v in over.items():
             setattr(a, k, v)
-        extra[name] = compact(fn(a, rank, world))
+        try:
+            extra[name] = compact(fn(a, rank, world))
+        except Exception as e:             # one failed extra must not cost the headline line
+            extra[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+            if world > 1:
+                raise
         torch.cuda.empty_cache()
     return extra
 
