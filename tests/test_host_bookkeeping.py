@@ -189,3 +189,37 @@ def test_special_policy_evict_arguments_must_match(kvc):
     assert (g.num_camera_pages, g.max_num_pages) == (3, 88 + 13 + 3)
     assert kvc.kvc_get_geometry(kvc.make_config(1, 16, 64, 999)).num_camera_pages == 0
     c.close()
+
+
+def test_free_pool_exhausted_by_deferred_frames(kvc):
+    """More provisional frames than the pool holds: with eviction deferred
+    the window keeps growing until no patch page is free; the next append
+    returns NO_FREE_PAGE and changes nothing; rolling the provisional frames
+    back restores the pool exactly (the same failure on the oracle)."""
+    lib = kvc.PagedKVCache(1, 2, 32, 16, "f32", 2, 4, 2, 64, device=None)
+    orc = OraclePagedKV(1, 16, 2, 32, "f32", 2, 4, 2, 64, mirror_blocks=())
+    z = np.zeros((22, 2, 32), np.uint32)
+    for _ in range(6):                           # scale 2 + window 4, committed
+        lib.append_frame(0); lib.evict_frames(0)
+        orc.append_frame(0, z, z); orc.evict_frames(0, 2, 4)
+    before = lib.deques(0)
+    lib.set_defer_eviction(True); orc.set_defer_eviction(True)
+    for _ in range(2):                           # headroom 2: the pool is now empty
+        lib.append_frame(0); lib.evict_frames(0)
+        orc.append_frame(0, z, z); orc.evict_frames(0, 2, 4)
+    full = (lib.deques(0), lib.stats(0))
+    assert full[1]["free_pages"] == 0
+    with pytest.raises(kvc.KvcError) as e:
+        lib.append_frame(0)
+    assert e.value.code == "NO_FREE_PAGE"
+    with pytest.raises(OracleError) as oe:
+        orc.append_frame(0, z, z)
+    assert oe.value.code == "NO_FREE_PAGE"
+    assert (lib.deques(0), lib.stats(0)) == full          # the failed call changed nothing
+    for _ in range(2):
+        lib.rollback_last_frame(0); orc.rollback_last_frame(0)
+    assert lib.deques(0) == before == tuple(orc.deques(0))
+    with pytest.raises(kvc.KvcError) as e:
+        lib.rollback_last_frame(0)
+    assert e.value.code == "NOTHING_TO_ROLLBACK"
+    lib.close()
