@@ -219,6 +219,12 @@ def test_free_pool_exhausted_by_deferred_frames(kvc):
     for _ in range(2):
         lib.rollback_last_frame(0); orc.rollback_last_frame(0)
     assert lib.deques(0) == before == tuple(orc.deques(0))
+    # No eviction has moved a page, so the first six frames are still
+    # uncommitted (an eviction commits only when it moves a page): rollback
+    # goes on undoing them, on both sides, until nothing is left.
+    for _ in range(6):
+        lib.rollback_last_frame(0); orc.rollback_last_frame(0)
+        assert lib.deques(0) == tuple(orc.deques(0)) and lib.stats(0) == orc.stats(0)
     with pytest.raises(kvc.KvcError) as e:
         lib.rollback_last_frame(0)
     assert e.value.code == "NOTHING_TO_ROLLBACK"
