@@ -299,10 +299,16 @@ enum {
   KVC_OPT_STALL_TEST = 5,  /* test only, 1: the tensor-core kernel first waits on a barrier
                               that nothing signals, so its bounded wait runs out and the run
                               reports KVC_ERR_DEVICE_TIMEOUT (no output is written)           */
-  KVC_OPT_QUERY_TILES = 6  /* tensor-core kernel: 128-row query tiles per CTA; 0 auto (a
+  KVC_OPT_QUERY_TILES = 6, /* tensor-core kernel: 128-row query tiles per CTA; 0 auto (a
                               cost model picks tiles and splits per launch), 1 (both softmax
                               warp groups share one tile, taking alternate KV tiles), 2 (one
                               warp group per tile)                                           */
+  KVC_OPT_PACK_TILES = 7   /* tensor-core kernel: 1 (default) packs the KV tiles across page
+                              boundaries in units of 8 rows -- a page's last tile is filled
+                              with the next page's first rows -- when every visible page but
+                              the last has at least 113 rows (otherwise the plan keeps one
+                              page per tile); 0 never packs.  Takes effect at the next
+                              kvc_plan.                                                      */
 };
 int kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
 
@@ -345,6 +351,11 @@ int kvc_paged_attention_static(const void* cache_block, int32_t dtype, int32_t n
  * with this handle first): 128-row query tiles per CTA of the tensor-core
  * kernel (0 for the CUDA-core kernel) and KV splits.  Diagnostics. */
 int kvc_get_launch_shape(const kvc_handle* h, int32_t* q_tiles, int32_t* splits);
+
+/* KV tiles of the current plan and whether they are packed (1: tiles of 128
+ * rows cross page boundaries, see KVC_OPT_PACK_TILES; 0: one page per tile).
+ * KVC_ERR_NO_PLAN before the first kvc_plan.  Diagnostics. */
+int kvc_get_plan_tiles(const kvc_handle* h, int32_t* n_tiles, int32_t* packed);
 
 /* Static message for a status code. */
 const char* kvc_strerror(int code);

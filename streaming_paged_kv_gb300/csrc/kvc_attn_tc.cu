@@ -5,11 +5,13 @@
 // What it computes ([KVC] "Kernel-Level Execution Flow": causal=False,
 // pos_encoding_mode="NONE", as many KV heads as query heads):
 //     O[t,h,:] = sum_j softmax_j(Q[t,h,:].K[j,h,:] * sm_scale) V[j,h,:]
-// over the visible tokens j, which the plan lists as KV tiles of at most 128
-// rows of one page (scale pages, live window, then the special pages; a
-// page's rows beyond its valid count never enter the softmax, so exact page
-// sizes such as 999 need no padding -- [PERF] "Page-Size Handling for FA2 vs
-// FA3").
+// over the visible tokens j, which the plan lists as KV tiles of 128 rows
+// (scale pages, live window, then the special pages; a page's rows beyond its
+// valid count never enter the softmax, so exact page sizes such as 999 need no
+// padding -- [PERF] "Page-Size Handling for FA2 vs FA3").  A tile holds rows of
+// one page, or -- packed -- a page's last rows rounded up to a multiple of 8
+// and the next page's first rows, gathered as 8-row boxes into the 1024-byte
+// swizzle atoms of the stage, so that a 999-row page costs 7.8 tiles, not 8.
 //
 // Pages cited by tag: [KVC] "How LingBot-Map Implements the KV Cache Mechanism
 // for Streaming Inference with FlashInfer Integration"; [PERF] "How to Improve
@@ -61,7 +63,8 @@
 namespace kvc {
 
 struct TcMaps {
-  CUtensorMap cache;     // 3D view of the whole cache: {H*D, page_size, blocks*pages*2}
+  CUtensorMap cache;     // 3D view of the whole cache: {H*D, page_size, blocks*pages*2}, 128-row boxes
+  CUtensorMap cache8;    // the same view with 8-row boxes (packed tiles)
   int dtype;
   int num_heads;
   int head_dim;
@@ -394,22 +397,28 @@ struct TcRequest {
   int32_t* status;
   int32_t n_tiles, n_splits, q_row0, n_q, page_base, cta0, q_blocks, max_pages, page_size;
 };
+// MAXB: requests the parameter block has room for -- 1 for single-stream
+// launches, which then pass about 0.6 KB of parameters instead of 5.4 KB.
+template <int MAXB>
 struct TcLaunch {
   CUtensorMap q_map;       // [rows, H * D] over every request's query rows
-  CUtensorMap cache_map[kTcMaxBatch];   // 3D view of each request's whole cache
+  CUtensorMap cache_map[MAXB];    // 3D view of each request's whole cache
+  CUtensorMap cache_map8[MAXB];   // the same with 8-row boxes
   void* out;               // [rows, H, D]
   int32_t count, num_heads, stall_test;
   int32_t allow_dual;      // single-query-tile CTAs may use dual mode (three or more waves of CTAs)
   int32_t q_rows_cta;      // query rows per CTA: 256 (two tiles) or 128 (one tile)
   float sm_scale_log2;
   long long wait_budget;
-  TcRequest req[kTcMaxBatch];
+  TcRequest req[MAXB];
 };
-static_assert(sizeof(TcLaunch) <= 4000, "kernel parameter space");
+// Above the classic 4 KB: kernel parameters may take up to 32764 bytes on
+// every architecture this file builds for (CUDA 12.1 and later).
+static_assert(sizeof(TcLaunch<kTcMaxBatch>) <= 32764, "kernel parameter space");
 
-template <bool BF16>
+template <bool BF16, int MAXB>
 __global__ void __launch_bounds__(REG_BOUND_THREADS, 1)
-attn_tc_kernel(const __grid_constant__ TcLaunch P) {
+attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + OFF_Q;
@@ -462,6 +471,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
   const int n_s = n * per_tile;                   // score tiles of this CTA
   const KvTile* tiles = R.tiles;
   const CUtensorMap* cache_map = &P.cache_map[rq];
+  const CUtensorMap* cache_map8 = &P.cache_map8[rq];
   Guard g{abort_flag, R.status, P.wait_budget};
 
   if (threadIdx.x == 0) {
@@ -510,16 +520,38 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
         if (j >= STAGES && !wait_bar_warp(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
         const KvTile tile = tiles[t0 + j];
         const int plane = (R.page_base + tile.page) * 2;
-        if (KVC_CHECKED && (tile.page < 0 || tile.page >= R.max_pages || tile.row0 < 0 || tile.rows < 1 ||
-                            tile.rows > BN || tile.row0 + tile.rows > R.page_size || h >= P.num_heads)) {
+        const int units1 = (tile.rows + 7) >> 3;        // 8-row units of the first segment
+        if (KVC_CHECKED &&
+            (tile.page < 0 || tile.page >= R.max_pages || tile.row0 < 0 || tile.rows < 1 || tile.rows > BN ||
+             tile.row0 + tile.rows > R.page_size || h >= P.num_heads ||
+             (tile.page2 < 0 ? tile.rows2 != 0
+                             : (tile.page2 >= R.max_pages || tile.row0_2 < 0 || tile.rows2 < 1 ||
+                                units1 * 8 + tile.rows2 > BN || tile.row0_2 + tile.rows2 > R.page_size)))) {
           if (leader) raise_bounds(g, 401, t0 + j);
           __syncwarp();
           break;
         }
         if (leader) {
           mbar_expect_tx(&kv_full[st], 2 * TILE_BYTES);
-          tma_load_3d(sK + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane, &kv_full[st]);
-          tma_load_3d(sV + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
+          if (tile.page2 < 0) {
+            tma_load_3d(sK + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane, &kv_full[st]);
+            tma_load_3d(sV + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
+          } else {
+            // Packed tile: 16 boxes of 8 rows, each into its own 1024-byte
+            // swizzle atom -- the first segment's units, then the second
+            // page's from its row0_2.  Units past the second segment's rows
+            // read rows past its valid count (masked in S; past the page end
+            // the copy fills zeros), so every byte of the stage is written.
+            const int plane2 = (R.page_base + tile.page2) * 2;
+#pragma unroll 1
+            for (int x = 0; x < BN / 8; ++x) {
+              const bool one = x < units1;
+              const int row = one ? tile.row0 + 8 * x : tile.row0_2 + 8 * (x - units1);
+              const int pl = one ? plane : plane2;
+              tma_load_3d(sK + st * TILE_BYTES + x * 1024, cache_map8, h * HD, row, pl, &kv_full[st]);
+              tma_load_3d(sV + st * TILE_BYTES + x * 1024, cache_map8, h * HD, row, pl + 1, &kv_full[st]);
+            }
+          }
         }
         issued = j + 1;
       }
@@ -653,21 +685,33 @@ attn_tc_kernel(const __grid_constant__ TcLaunch P) {
     // tiles qi, qi + 2, ..., otherwise every KV tile.
     const int n_g = dual ? (n - qi + 1) / 2 : n;
 
-    int rows_next = ok ? tiles[t0 + (dual ? qi : 0)].rows : 0;
+    // Valid rows of a tile: {rows, rows2} -- the first segment's rows, then
+    // (packed tiles) the second's from row ceil(rows / 8) * 8.
+    // Both (at most 128) travel in one register: rows | rows2 << 8.
+    auto tile_rows = [&](int t) {
+      const int2 r = *reinterpret_cast<const int2*>(&tiles[t].rows);
+      return r.x | (r.y << 8);
+    };
+    int rows_next = ok ? tile_rows(t0 + (dual ? qi : 0)) : 0;
     for (int j = 0; ok && j < n_g; ++j) {
       const int k = j * groups + qi, b = k % NBUF;
       const int rows_valid = rows_next;
-      if (j + 1 < n_g) rows_next = tiles[t0 + (dual ? k + 2 : j + 1)].rows;   // prefetch for the next tile
+      if (j + 1 < n_g) rows_next = tile_rows(t0 + (dual ? k + 2 : j + 1));   // prefetch for the next tile
       ok = wait_bar_warp(g, &s_full[b], (k / NBUF) & 1, 6);
       if (!ok) break;
       tc_fence_after();
       const uint32_t S_ = lane_base + buf_col(b);
-      if (rows_valid < BN) {
-        // Rows of the tile past its valid count never enter the softmax: their
-        // scores are overwritten with -inf in TMEM before the row is read
-        // (a short loop keeps this rare case out of the unrolled hot path).
+      const int rows1 = rows_valid & 0xff, rows2 = rows_valid >> 8;
+      if (rows1 + rows2 < BN) {
+        // Rows of the tile that hold no visible token never enter the softmax:
+        // their scores are overwritten with -inf in TMEM before the row is
+        // read (short loops keep this rare case out of the unrolled hot path).
+        // They are [rows, ceil8(rows)) and [ceil8(rows) + rows2, BN).
         const uint32_t ninf = __float_as_uint(-INFINITY);
-        int c = rows_valid;
+        const int a8 = (rows1 + 7) & ~7;
+        int c = rows1;
+        for (; c < a8; ++c) tmem_st1(S_ + c, ninf);
+        c = a8 + rows2;
         for (; (c & 7) != 0; ++c) tmem_st1(S_ + c, ninf);
         for (; c < BN; c += 8) tmem_st8(S_ + c, ninf);
         tmem_wait_st();
@@ -865,7 +909,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool configured_smem[2] = {false, false};
+bool configured_smem[4] = {false, false, false, false};
 
 }  // namespace
 
@@ -893,10 +937,14 @@ TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, in
                         (cuuint64_t)num_blocks * max_pages * 2};
   cuuint64_t strides[2] = {row_bytes, row_bytes * page_size};
   cuuint32_t box[3] = {HD, BN, 1};
+  cuuint32_t box8[3] = {HD, 8, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(&m->cache, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                   cache, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType ty = dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(&m->cache, ty, 3, cache, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS)
+    r = enc(&m->cache8, ty, 3, cache, dims, strides, box8, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     delete m;
     if (err) *err = cudaErrorInvalidValue;
@@ -907,11 +955,11 @@ TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, in
 
 void tc_destroy_maps(TcMaps* m) { delete m; }
 
-cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc || b.count < 1 || b.count > kTcMaxBatch || b.head_dim != HD) return cudaErrorNotSupported;
-  if (b.q_tiles != 1 && b.q_tiles != QT) return cudaErrorInvalidValue;
-  TcLaunch P;
+namespace {
+
+template <int MAXB>
+cudaError_t launch_impl(const TcBatchArgs& b, EncodeTiledFn enc, cudaStream_t stream) {
+  TcLaunch<MAXB> P;
   std::memset(&P, 0, sizeof(P));
   const cuuint64_t row_bytes = (cuuint64_t)b.num_heads * HD * 2;
   cuuint64_t dims[2] = {(cuuint64_t)b.num_heads * HD, (cuuint64_t)b.rows};
@@ -936,6 +984,7 @@ cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     TcRequest& q = P.req[r];
     P.cache_map[r] = d.maps->cache;
+    P.cache_map8[r] = d.maps->cache8;
     q.tiles = d.tiles;
     q.part_o = d.part_o;
     q.part_lse = d.part_lse;
@@ -956,8 +1005,8 @@ cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
   // waves on (measured).  One-tile CTAs always run in dual mode.
   P.allow_dual = (b.q_tiles == 1 || ctas > 2 * (int64_t)b.num_sms) ? 1 : 0;
   if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
-  const int which = b.dtype == 0 ? 0 : 1;
-  auto kernel = which == 0 ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  const int which = (b.dtype == 0 ? 0 : 1) + (MAXB == 1 ? 0 : 2);
+  auto kernel = b.dtype == 0 ? attn_tc_kernel<true, MAXB> : attn_tc_kernel<false, MAXB>;
   if (!configured_smem[which]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -965,6 +1014,15 @@ cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
   }
   kernel<<<(unsigned)ctas, NUM_THREADS, SMEM_BYTES, stream>>>(P);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const TcBatchArgs& b, cudaStream_t stream) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || b.count < 1 || b.count > kTcMaxBatch || b.head_dim != HD) return cudaErrorNotSupported;
+  if (b.q_tiles != 1 && b.q_tiles != QT) return cudaErrorInvalidValue;
+  return b.count == 1 ? launch_impl<1>(b, enc, stream) : launch_impl<kTcMaxBatch>(b, enc, stream);
 }
 
 }  // namespace kvc

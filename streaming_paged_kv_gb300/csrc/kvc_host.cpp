@@ -163,6 +163,7 @@ struct kvc_handle {
   // Plan (host copy + the state it was made from).
   bool has_plan = false;
   int32_t plan_n_pages = 0, plan_lpl = 0, plan_n_tiles = 0, plan_tile_rows = 0, plan_kernel = 0;
+  bool plan_packed = false;
   int32_t plan_n_scale = 0, plan_n_live = 0, plan_special_frames = 0;
   int32_t* plan_ids = nullptr;      // [max_entries]
   int32_t* plan_row0 = nullptr;     // [max_entries]
@@ -173,6 +174,7 @@ struct kvc_handle {
   int opt_kernel = 0;
   int opt_splits = 0;
   int opt_qtiles = 0;
+  bool opt_pack = true;
   long long wait_budget = 0;
   bool timing = false;
   int stall_test = 0;
@@ -646,22 +648,32 @@ int kvc_plan(kvc_handle* h, kvc_stream stream) {
   for (int32_t i = 0; i < n_scale; ++i) a.patch_ids[i] = b.scale.at(i);
   for (int32_t i = 0; i < n_live; ++i) a.patch_ids[n_scale + i] = b.live.at(i);
   // Host copy of the visible entries (the device plan kernel writes the same).
-  int64_t n_tiles = 0;
   int32_t e = 0;
   for (; e < n_patch; ++e) {
     h->plan_ids[e] = a.patch_ids[e];
     h->plan_row0[e] = 0;
     h->plan_valid[e] = h->cfg.page_size;
-    n_tiles += (h->cfg.page_size + tr - 1) / tr;
   }
   for (int r = 0; r < a.n_runs; ++r) {
     const int32_t n = kvc::run_pages(a.runs[r]);
-    for (int32_t i = 0; i < n; ++i, ++e) {
+    for (int32_t i = 0; i < n; ++i, ++e)
       kvc::run_entry(a.runs[r], i, &h->plan_ids[e], &h->plan_row0[e], &h->plan_valid[e]);
-      n_tiles += (h->plan_valid[e] + tr - 1) / tr;
-    }
   }
+  // Tensor-core plans pack tiles in 8-row units when no tile can span more
+  // than two entries; the count is ceil(units / 16), never more than one page
+  // per tile gives.
+  constexpr int32_t U = kvc::kPackUnitRows;
+  bool pack = kernel == 2 && h->opt_pack && tr == kvc::kTcTileRows;
+  int64_t units = 0, n_tiles = 0;
+  for (int32_t i = 0; i < n_pages; ++i) {
+    const int32_t u = (h->plan_valid[i] + U - 1) / U;
+    if (i + 1 < n_pages && u < kvc::kPackMinUnits) pack = false;
+    units += u;
+    n_tiles += (h->plan_valid[i] + tr - 1) / tr;
+  }
+  if (pack) n_tiles = (units + tr / U - 1) / (tr / U);
   if (n_tiles > h->g.L.max_tiles) return KVC_ERR_INVALID_ARG;
+  a.pack = pack ? 1 : 0;
   if (h->device) {
     cudaError_t err = kvc::launch_plan(a, h->ws, h->g.L, (cudaStream_t)stream);
     if (err != cudaSuccess) return KVC_ERR_CUDA;
@@ -676,6 +688,7 @@ int kvc_plan(kvc_handle* h, kvc_stream stream) {
   // page's tokens ([KVC] "Physical Page Layout and Indexing").
   h->plan_lpl = h->plan_valid[n_pages - 1];
   h->plan_n_tiles = (int32_t)n_tiles;
+  h->plan_packed = pack;
   h->plan_tile_rows = tr;
   h->plan_kernel = kernel;
   h->has_plan = true;
@@ -975,6 +988,11 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
       if (value < 0 || value > 2) return KVC_ERR_INVALID_ARG;
       h->opt_qtiles = (int)value;
       return KVC_OK;
+    case KVC_OPT_PACK_TILES:
+      if (value < 0 || value > 1) return KVC_ERR_INVALID_ARG;
+      h->opt_pack = value != 0;
+      h->has_plan = false;      // the tile list changes
+      return KVC_OK;
     case KVC_OPT_WAIT_BUDGET:
       if (value < 0) return KVC_ERR_INVALID_ARG;
       h->wait_budget = value;
@@ -1019,6 +1037,14 @@ int kvc_get_counters(kvc_handle* h, int64_t* kernel_launches, int64_t* attn_laun
     h->attn_launches = 0;
     h->attn_ms = 0.0;
   }
+  return KVC_OK;
+}
+
+int kvc_get_plan_tiles(const kvc_handle* h, int32_t* n_tiles, int32_t* packed) {
+  if (!h) return KVC_ERR_INVALID_ARG;
+  if (!h->has_plan) return KVC_ERR_NO_PLAN;
+  if (n_tiles) *n_tiles = h->plan_n_tiles;
+  if (packed) *packed = h->plan_packed ? 1 : 0;
   return KVC_OK;
 }
 

@@ -45,13 +45,28 @@ struct DevPlanHeader {
   int32_t n_tokens;
 };
 
-// One KV tile of a visible page: rows [row0, row0 + rows) of page `page`.
-struct KvTile {
+// One KV tile: rows [row0, row0 + rows) of page `page`, and in a packed tile
+// (tensor-core plans, page2 >= 0) rows [row0_2, row0_2 + rows2) of page2 after
+// them, from tile row ceil(rows / 8) * 8 on; rows2 = 0 and page2 = -1 otherwise.
+struct alignas(16) KvTile {
   int32_t page;
   int32_t row0;
   int32_t rows;
+  int32_t rows2;   // next to rows: the softmax reads both with one 8-byte load
+  int32_t page2;
+  int32_t row0_2;
   int32_t token0;  // position of the tile's first token in the visible sequence
+  int32_t pad;
 };
+static_assert(sizeof(KvTile) == 32, "KvTile layout");
+
+// Packed tiles are built from units of 8 rows (the 128-byte swizzle atom of a
+// 64-wide bf16 row): a visible entry of v rows takes ceil(v / 8) units, and
+// tile t covers units [16 t, 16 t + 16) of the concatenated entries.  A tile
+// then spans at most two entries when every entry but the last has at least
+// kPackMinUnits units.
+constexpr int kPackUnitRows = 8;
+constexpr int kPackMinUnits = 15;
 
 // Workspace layout (byte offsets from the workspace base).
 struct WorkspaceLayout {
@@ -101,6 +116,7 @@ struct PlanArgs {
   PlanRun runs[kMaxRuns];
   int32_t page_size;
   int32_t tile_rows;                // rows per KV tile of the attention kernel
+  int32_t pack;                     // 1: packed tiles of tile_rows rows in 8-row units
   int32_t max_pages;                // pages of one block's cache (bounds checks)
   int32_t patch_ids[kMaxPatchPages];
 };

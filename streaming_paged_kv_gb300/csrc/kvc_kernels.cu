@@ -62,65 +62,112 @@ __global__ void append_kernel(char* __restrict__ cache_block, const char* __rest
 // ([KVC] "Patch Pages vs. Special Pages"; [SLOTS] "双流分页布局").  With the
 // default special policy there is one run, every special page from row 0, a
 // non-last page holding 6*fpp tokens and the last last_page_len.
+
+__device__ __forceinline__ int32_t cdiv(int32_t x, int32_t u) { return (x + u - 1) / u; }
+
+// Entry e of the visible list: page id, first row, valid rows, and where it
+// starts in units of u rows (every entry rounded up to whole units) and in
+// tokens.  Only a run's first and last page can be partial, so the offsets
+// have a closed form.  e == the entry count gives the totals (id -1).
+struct PlanEntry {
+  int32_t id, row0, v, unit0, token0;
+};
+
+__device__ PlanEntry plan_entry(const PlanArgs& a, int32_t e, int32_t u) {
+  PlanEntry x;
+  if (e < a.n_patch) {
+    x.id = a.patch_ids[e];
+    x.row0 = 0;
+    x.v = a.page_size;
+    x.unit0 = e * cdiv(a.page_size, u);
+    x.token0 = e * a.page_size;
+    return x;
+  }
+  int32_t entry = a.n_patch, unit = a.n_patch * cdiv(a.page_size, u), token = a.n_patch * a.page_size;
+  for (int32_t r = 0; r < a.n_runs; ++r) {
+    const PlanRun& run = a.runs[r];
+    const int32_t n = run_pages(run);
+    if (n == 0) continue;
+    int32_t id, row0, v0, vf, vl;
+    run_entry(run, 0, &id, &row0, &v0);
+    run_entry(run, n > 1 ? 1 : 0, &id, &row0, &vf);
+    if (e < entry + n) {
+      const int32_t k = e - entry;
+      run_entry(run, k, &x.id, &x.row0, &x.v);
+      x.unit0 = unit + (k == 0 ? 0 : cdiv(v0, u) + (k - 1) * cdiv(vf, u));
+      x.token0 = token + (k == 0 ? 0 : v0 + (k - 1) * vf);
+      return x;
+    }
+    run_entry(run, n - 1, &id, &row0, &vl);
+    unit += n == 1 ? cdiv(v0, u) : cdiv(v0, u) + (n - 2) * cdiv(vf, u) + cdiv(vl, u);
+    token += n == 1 ? v0 : v0 + (n - 2) * vf + vl;
+    entry += n;
+  }
+  x.id = -1;
+  x.row0 = x.v = 0;
+  x.unit0 = unit;
+  x.token0 = token;
+  return x;
+}
+
+// Tiles: without packing, every entry is cut into tiles of tile_rows rows.
+// Packed (tensor-core plans whose entries but the last have >= 15 units of 8
+// rows): tile t covers units [16 t, 16 t + 16) of the concatenated entries;
+// the entry holding unit 16 t writes it -- its own rows from there, and, if
+// the tile has room left, the next entry's first rows.
 __global__ void plan_kernel(const __grid_constant__ PlanArgs a, char* __restrict__ ws,
                             WorkspaceLayout L) {
   const int32_t tr = a.tile_rows;
-  const int32_t tpp = (a.page_size + tr - 1) / tr;
+  const int32_t u = a.pack ? kPackUnitRows : tr;     // unit of the tile offsets
+  const int32_t per_tile = tr / u;                   // units per tile
   int32_t* ids = reinterpret_cast<int32_t*>(ws + L.page_ids);
   int32_t* valid = reinterpret_cast<int32_t*>(ws + L.page_valid);
   int32_t* first = reinterpret_cast<int32_t*>(ws + L.page_row0);
   KvTile* tiles = reinterpret_cast<KvTile*>(ws + L.tiles);
-  auto emit = [&](int32_t i, int32_t id, int32_t row0, int32_t v, int32_t tile0, int32_t token0) {
-    if (KVC_CHECKED && (i < 0 || i >= L.max_pages || id < 0 || id >= a.max_pages || row0 < 0 || v < 1 ||
-                        row0 + v > a.page_size || tile0 < 0 || tile0 + (v + tr - 1) / tr > L.max_tiles)) {
-      record_bounds(reinterpret_cast<int32_t*>(ws + L.status), 201, i);
-      return;
+  int32_t n_entries = a.n_patch;
+  for (int32_t r = 0; r < a.n_runs; ++r) n_entries += run_pages(a.runs[r]);
+  const PlanEntry end = plan_entry(a, n_entries, u);
+  const int32_t n_tiles = cdiv(end.unit0, per_tile);
+  for (int32_t e = threadIdx.x; e < n_entries; e += blockDim.x) {
+    const PlanEntry x = plan_entry(a, e, u);
+    const int32_t t_lo = cdiv(x.unit0, per_tile), t_hi = cdiv(x.unit0 + cdiv(x.v, u), per_tile);
+    if (KVC_CHECKED && (e >= L.max_pages || x.id < 0 || x.id >= a.max_pages || x.row0 < 0 || x.v < 1 ||
+                        x.row0 + x.v > a.page_size || t_hi > L.max_tiles)) {
+      record_bounds(reinterpret_cast<int32_t*>(ws + L.status), 201, e);
+      continue;
     }
-    ids[i] = id;
-    valid[i] = v;
-    first[i] = row0;
-    for (int32_t t = 0, r = 0; r < v; ++t, r += tr) {
+    ids[e] = x.id;
+    valid[e] = x.v;
+    first[e] = x.row0;
+    PlanEntry y;
+    y.id = -1;
+    if (a.pack && e + 1 < n_entries) y = plan_entry(a, e + 1, u);
+    for (int32_t t = t_lo; t < t_hi; ++t) {
+      const int32_t r0 = (t * per_tile - x.unit0) * u;   // first row of the tile within the entry
       KvTile k;
-      k.page = id;
-      k.row0 = row0 + r;
-      k.rows = min(tr, v - r);
-      k.token0 = token0 + r;
-      tiles[tile0 + t] = k;
+      k.page = x.id;
+      k.row0 = x.row0 + r0;
+      k.rows = min(tr, x.v - r0);
+      k.token0 = x.token0 + r0;
+      k.page2 = -1;
+      k.row0_2 = 0;
+      k.rows2 = 0;
+      k.pad = 0;
+      const int32_t room = tr - cdiv(k.rows, u) * u;    // packed: rows left after whole units
+      if (a.pack && room > 0 && y.id >= 0) {
+        k.page2 = y.id;
+        k.row0_2 = y.row0;
+        k.rows2 = min(room, y.v);
+      }
+      tiles[t] = k;
     }
-  };
-  for (int32_t i = threadIdx.x; i < a.n_patch; i += blockDim.x)
-    emit(i, a.patch_ids[i], 0, a.page_size, i * tpp, i * a.page_size);
-  // Runs: page e of a run starts after the run's earlier pages; only a run's
-  // first and last page can be partial, so the offsets have a closed form.
-  int32_t entry = a.n_patch, tile = a.n_patch * tpp, token = a.n_patch * a.page_size;
-  int32_t last_valid = a.n_patch > 0 ? a.page_size : 0;
-  for (int32_t r = 0; r < a.n_runs; ++r) {
-    const PlanRun& run = a.runs[r];
-    const int32_t n = run_pages(run);
-    int32_t id, row0, v0, vf, vl;
-    run_entry(run, 0, &id, &row0, &v0);
-    run_entry(run, n > 1 ? 1 : 0, &id, &row0, &vf);
-    run_entry(run, n - 1, &id, &row0, &vl);
-    const int32_t t0 = (v0 + tr - 1) / tr, tf = (vf + tr - 1) / tr;
-    for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
-      int32_t v;
-      run_entry(run, e, &id, &row0, &v);
-      emit(entry + e, id, row0, v, tile + (e == 0 ? 0 : t0 + (e - 1) * tf),
-           token + (e == 0 ? 0 : v0 + (e - 1) * vf));
-    }
-    if (n > 0) {
-      tile += n == 1 ? t0 : t0 + (n - 2) * tf + (vl + tr - 1) / tr;
-      token += n == 1 ? v0 : v0 + (n - 2) * vf + vl;
-      last_valid = vl;
-    }
-    entry += n;
   }
   if (threadIdx.x == 0) {
     DevPlanHeader h;
-    h.n_pages = entry;
-    h.last_page_len = last_valid;
-    h.n_tiles = tile;
-    h.n_tokens = token;
+    h.n_pages = n_entries;
+    h.last_page_len = n_entries > 0 ? plan_entry(a, n_entries - 1, u).v : 0;
+    h.n_tiles = n_tiles;
+    h.n_tokens = end.token0;
     *reinterpret_cast<DevPlanHeader*>(ws + L.header) = h;
   }
 }

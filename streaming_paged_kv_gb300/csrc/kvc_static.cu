@@ -104,6 +104,10 @@ __global__ void static_tiles_kernel(const __grid_constant__ StaticPages p, KvTil
       k.row0 = r0;
       k.rows = min(p.tile_rows, p.valid[i] - r0);
       k.token0 = token0 + r0;
+      k.page2 = -1;
+      k.row0_2 = 0;
+      k.rows2 = 0;
+      k.pad = 0;
       tiles[p.tile0[i] + t] = k;
     }
   }

@@ -34,6 +34,7 @@ ERRORS = {
 }
 KVC_OPT_ATTN_KERNEL, KVC_OPT_NUM_SPLITS, KVC_OPT_WAIT_BUDGET, KVC_OPT_TIMING, KVC_OPT_STALL_TEST = 1, 2, 3, 4, 5
 KVC_OPT_QUERY_TILES = 6
+KVC_OPT_PACK_TILES = 7
 
 try:
     _DEBUG_EVERY = max(0, int(os.environ.get("KVC_DEBUG", "0") or 0))   # see PagedKVCache.plan
@@ -107,6 +108,7 @@ _SIGS = {
     "kvc_get_counters": [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                          ctypes.POINTER(ctypes.c_double), _I32],
     "kvc_get_launch_shape": [_P, _PI32, _PI32],
+    "kvc_get_plan_tiles": [_P, _PI32, _PI32],
     "kvc_paged_attention_static": [_P, _I32, _I32, _I32, _I32, _PI32, _PI32, _I32, _P, _P, _I32,
                                    ctypes.c_float, _P],
 }
@@ -310,6 +312,13 @@ def kvc_get_launch_shape(h):
     qt, sp = ctypes.c_int32(), ctypes.c_int32()
     _check(lib.kvc_get_launch_shape(h, ctypes.byref(qt), ctypes.byref(sp)), "kvc_get_launch_shape")
     return qt.value, sp.value
+
+
+def kvc_get_plan_tiles(h):
+    """(KV tiles, packed) of the handle's current plan."""
+    n, packed = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.kvc_get_plan_tiles(h, ctypes.byref(n), ctypes.byref(packed)), "kvc_get_plan_tiles")
+    return n.value, bool(packed.value)
 
 
 def kvc_strerror(rc):

@@ -47,6 +47,8 @@ class ParityEngine:
         self.check_bytes = check_bytes
         self.check_device_plan = check_device_plan
         self.results = []        # (frame, block, max_abs, rel_rms)
+        self.plans = []          # (frame, (n_tiles, packed), oracle visible ranges) at checked frames
+        self._plan = None
         self._q = {}
 
     def _inputs(self, b, f):
@@ -89,6 +91,7 @@ class ParityEngine:
 
     def plan(self):
         self.c.plan()
+        self._plan = (self.kvc.kvc_get_plan_tiles(self.c.h), tuple(self.orc.visible_ranges(0)))
         if self.check_device_plan:
             idx, valid, lpl = self.kvc.kvc_read_device_plan(self.c.h, self.c._stream())
             o_idx, _, o_lpl, o_valid = self.orc.visible_page_table(0)
@@ -103,6 +106,8 @@ class ParityEngine:
         out = torch.empty_like(qd)
         self.c.run(b, qd, out)
         if f in self.check_frames and b in self.orc.mirror:
+            if not self.plans or self.plans[-1][0] != f:
+                self.plans.append((f,) + self._plan)
             want = paged_attention(self.orc, b, to_bits(q), rows=self.rows)
             got = out if self.rows is None else out[torch.as_tensor(self.rows, device=out.device)]
             torch.cuda.synchronize()
