@@ -10,8 +10,9 @@
 // valid count never enter the softmax, so exact page sizes such as 999 need no
 // padding -- [PERF] "Page-Size Handling for FA2 vs FA3").  A tile holds rows of
 // one page, or -- packed -- a page's last rows rounded up to a multiple of 8
-// and the next page's first rows, gathered as 8-row boxes into the 1024-byte
-// swizzle atoms of the stage, so that a 999-row page costs 7.8 tiles, not 8.
+// and the next page's first rows, gathered as boxes of 8 to 64 rows into the
+// 1024-byte swizzle atoms of the stage, so that a 999-row page costs 7.8
+// tiles, not 8.
 //
 // Pages cited by tag: [KVC] "How LingBot-Map Implements the KV Cache Mechanism
 // for Streaming Inference with FlashInfer Integration"; [PERF] "How to Improve
@@ -64,7 +65,7 @@ namespace kvc {
 
 struct TcMaps {
   CUtensorMap cache;     // 3D view of the whole cache: {H*D, page_size, blocks*pages*2}, 128-row boxes
-  CUtensorMap cache8;    // the same view with 8-row boxes (packed tiles)
+  CUtensorMap cache_u[4];  // the same view with boxes of 8, 16, 32 and 64 rows (packed tiles)
   int dtype;
   int num_heads;
   int head_dim;
@@ -192,13 +193,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint64_t* bar) {
+// 3-D tile load with an L2 cache policy (createpolicy) for the copied lines.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                 uint64_t* bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// L2 policy that makes the lines it touches the first to be evicted.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -398,12 +407,12 @@ struct TcRequest {
   int32_t n_tiles, n_splits, q_row0, n_q, page_base, cta0, q_blocks, max_pages, page_size;
 };
 // MAXB: requests the parameter block has room for -- 1 for single-stream
-// launches, which then pass about 0.6 KB of parameters instead of 5.4 KB.
+// launches, which then pass about 0.9 KB of parameters instead of 11.6 KB.
 template <int MAXB>
 struct TcLaunch {
   CUtensorMap q_map;       // [rows, H * D] over every request's query rows
   CUtensorMap cache_map[MAXB];    // 3D view of each request's whole cache
-  CUtensorMap cache_map8[MAXB];   // the same with 8-row boxes
+  CUtensorMap cache_map_u[MAXB][4];  // the same with 8-, 16-, 32- and 64-row boxes
   void* out;               // [rows, H, D]
   int32_t count, num_heads, stall_test;
   int32_t allow_dual;      // single-query-tile CTAs may use dual mode (three or more waves of CTAs)
@@ -471,7 +480,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
   const int n_s = n * per_tile;                   // score tiles of this CTA
   const KvTile* tiles = R.tiles;
   const CUtensorMap* cache_map = &P.cache_map[rq];
-  const CUtensorMap* cache_map8 = &P.cache_map8[rq];
+  const CUtensorMap* maps_u = P.cache_map_u[rq];
   Guard g{abort_flag, R.status, P.wait_budget};
 
   if (threadIdx.x == 0) {
@@ -509,6 +518,11 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
     // The whole warp runs the loop and its waits; one elected lane issues.
     if (n > 0) {
       const bool leader = elect_one();
+      // K/V lines are read by the CTAs of one head and split at about the
+      // same time and never again in this launch, so they are loaded
+      // evict-first: the split-KV partials written meanwhile stay in L2 for
+      // the merge instead of going out to HBM and back.
+      const uint64_t kv_policy = policy_evict_first();
       int issued = 0;
       if (leader) {
         mbar_expect_tx(q_full, nq * Q_BYTES);
@@ -534,23 +548,30 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
         if (leader) {
           mbar_expect_tx(&kv_full[st], 2 * TILE_BYTES);
           if (tile.page2 < 0) {
-            tma_load_3d(sK + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane, &kv_full[st]);
-            tma_load_3d(sV + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane + 1, &kv_full[st]);
+            tma_load_3d_hint(sK + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane, &kv_full[st], kv_policy);
+            tma_load_3d_hint(sV + st * TILE_BYTES, cache_map, h * HD, tile.row0, plane + 1, &kv_full[st], kv_policy);
           } else {
-            // Packed tile: 16 boxes of 8 rows, each into its own 1024-byte
-            // swizzle atom -- the first segment's units, then the second
-            // page's from its row0_2.  Units past the second segment's rows
-            // read rows past its valid count (masked in S; past the page end
-            // the copy fills zeros), so every byte of the stage is written.
-            const int plane2 = (R.page_base + tile.page2) * 2;
-#pragma unroll 1
-            for (int x = 0; x < BN / 8; ++x) {
-              const bool one = x < units1;
-              const int row = one ? tile.row0 + 8 * x : tile.row0_2 + 8 * (x - units1);
-              const int pl = one ? plane : plane2;
-              tma_load_3d(sK + st * TILE_BYTES + x * 1024, cache_map8, h * HD, row, pl, &kv_full[st]);
-              tma_load_3d(sV + st * TILE_BYTES + x * 1024, cache_map8, h * HD, row, pl + 1, &kv_full[st]);
-            }
+            // Packed tile: the first segment's units (8 rows each) at units
+            // [0, units1) of the stage, then the second page's from its row0_2
+            // at units [units1, 16).  Each segment (1 to 15 units) is copied as
+            // boxes of 8, 4, 2 and 1 units, largest first, every box starting on
+            // a 1024-byte swizzle atom.  Units past the second segment's rows
+            // read rows past its valid count (masked in S; past the page end the
+            // copy fills zeros), so every byte of the stage is written.
+            auto load_units = [&](int unit, int count, int row, int pl) {
+#pragma unroll
+              for (int m = 3; m >= 0; --m) {
+                if (count & (1 << m)) {
+                  const uint32_t off = st * TILE_BYTES + unit * 1024;
+                  tma_load_3d_hint(sK + off, &maps_u[m], h * HD, row, pl, &kv_full[st], kv_policy);
+                  tma_load_3d_hint(sV + off, &maps_u[m], h * HD, row, pl + 1, &kv_full[st], kv_policy);
+                  unit += 1 << m;
+                  row += 8 << m;
+                }
+              }
+            };
+            load_units(0, units1, tile.row0, plane);
+            load_units(units1, BN / 8 - units1, tile.row0_2, (R.page_base + tile.page2) * 2);
           }
         }
         issued = j + 1;
@@ -937,14 +958,15 @@ TcMaps* tc_create_maps(void* cache, int dtype, int num_blocks, int max_pages, in
                         (cuuint64_t)num_blocks * max_pages * 2};
   cuuint64_t strides[2] = {row_bytes, row_bytes * page_size};
   cuuint32_t box[3] = {HD, BN, 1};
-  cuuint32_t box8[3] = {HD, 8, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType ty = dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = enc(&m->cache, ty, 3, cache, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r == CUDA_SUCCESS)
-    r = enc(&m->cache8, ty, 3, cache, dims, strides, box8, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  for (int u = 0; u < 4 && r == CUDA_SUCCESS; ++u) {
+    cuuint32_t box_u[3] = {HD, (cuuint32_t)(8 << u), 1};
+    r = enc(&m->cache_u[u], ty, 3, cache, dims, strides, box_u, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) {
     delete m;
     if (err) *err = cudaErrorInvalidValue;
@@ -984,7 +1006,7 @@ cudaError_t launch_impl(const TcBatchArgs& b, EncodeTiledFn enc, cudaStream_t st
       return cudaErrorInvalidValue;
     TcRequest& q = P.req[r];
     P.cache_map[r] = d.maps->cache;
-    P.cache_map8[r] = d.maps->cache8;
+    for (int u = 0; u < 4; ++u) P.cache_map_u[r][u] = d.maps->cache_u[u];
     q.tiles = d.tiles;
     q.part_o = d.part_o;
     q.part_lse = d.part_lse;
