@@ -210,6 +210,29 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Tile stores from shared memory (bulk-group completion).  Rows outside the
+// tensor are not written.  The source may be reused once wait_group.read has
+// returned; the writes themselves are complete when the grid is.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Generic-proxy writes to shared memory become visible to the copy engine.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -303,6 +326,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 // Named barrier over the eight softmax warps.
 __device__ __forceinline__ void softmax_sync(int id) {
   asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
+}
+
+// Named barrier over one softmax group's four warps (ids 3 and 4); the
+// second form also returns whether `pred` holds in all 128 threads.
+__device__ __forceinline__ void group_sync(int qi) {
+  asm volatile("bar.sync %0, 128;" ::"r"(3 + qi) : "memory");
+}
+__device__ __forceinline__ bool group_all(bool pred, int qi) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(3 + qi)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
@@ -413,6 +454,8 @@ struct TcLaunch {
   CUtensorMap q_map;       // [rows, H * D] over every request's query rows
   CUtensorMap cache_map[MAXB];    // 3D view of each request's whole cache
   CUtensorMap cache_map_u[MAXB][4];  // the same with 8-, 16-, 32- and 64-row boxes
+  CUtensorMap out_map[MAXB];      // one split: the request's output rows [n_q, H * D], 128 x 64 boxes
+  CUtensorMap part_map[MAXB];     // several splits: its partials [n_splits][n_q][H * D] fp32, 128 x 32 boxes
   void* out;               // [rows, H, D]
   int32_t count, num_heads, stall_test;
   int32_t allow_dual;      // single-query-tile CTAs may use dual mode (three or more waves of CTAs)
@@ -851,7 +894,13 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
           good = false;
         }
       }
-      if (good) {
+      // Output: the group's 128 rows are staged in shared memory -- its own Q
+      // tile, free once its last S product has completed (in dual mode group
+      // 0 writes, after both groups' S products) -- in the 128-byte swizzle,
+      // and leave as TMA stores of whole row segments (the copy clips rows
+      // past n_q), instead of 16-byte stores scattered over 128 rows.  The
+      // group's four warps first agree that all of them got here in order.
+      if (group_all(good, qi)) {
         tc_fence_after();
         uint32_t v[HD];
         tmem_ld32_at<0>(O_, v);
@@ -870,29 +919,46 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
             v[c] = __float_as_uint(fmaf(w1, __uint_as_float(v1[c]), w0 * __uint_as_float(v[c])));
         }
         const int row = q0 + qi * BM + r;             // within the request
-        if (row < R.n_q) {
-          const float inv = 1.f / l;
-          if (R.n_splits == 1) {
-            using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(P.out) +
-                                                  ((int64_t)(R.q_row0 + row) * P.num_heads + h) * HD);
+        const float inv = 1.f / l;
+        uint8_t* stage = sQ + qi * Q_BYTES;           // 128 rows x 128 bytes
+        const uint32_t srow = smem_u32(stage) + r * 128;
+        const bool issuer = (warp & 3) == 0 && lane == 0;
+        if (R.n_splits == 1) {
+          // 64 16-bit values per row: eight 16-byte chunks, chunk c at c ^ (r mod 8).
 #pragma unroll
-            for (int i = 0; i < HD / 8; ++i) {
-              const float* o = reinterpret_cast<const float*>(&v[8 * i]);
-              uint4 u;
-              u.x = pack2<BF16>(o[0] * inv, o[1] * inv);
-              u.y = pack2<BF16>(o[2] * inv, o[3] * inv);
-              u.z = pack2<BF16>(o[4] * inv, o[5] * inv);
-              u.w = pack2<BF16>(o[6] * inv, o[7] * inv);
-              dst[i] = u;
+          for (int c = 0; c < HD / 8; ++c) {
+            const float* o = reinterpret_cast<const float*>(&v[8 * c]);
+            st_shared16(srow + ((c ^ (r & 7)) << 4), pack2<BF16>(o[0] * inv, o[1] * inv),
+                        pack2<BF16>(o[2] * inv, o[3] * inv), pack2<BF16>(o[4] * inv, o[5] * inv),
+                        pack2<BF16>(o[6] * inv, o[7] * inv));
+          }
+          fence_proxy_async();
+          group_sync(qi);
+          if (issuer) {
+            tma_store_2d(&P.out_map[rq], stage, h * HD, q0 + qi * BM);
+            bulk_commit();
+            bulk_wait_read();
+          }
+        } else {
+          if (row < R.n_q) R.part_lse[((int64_t)split * R.n_q + row) * P.num_heads + h] = m_fin + __log2f(l);
+          // 64 fp32 values per row: two halves of 32 (128 bytes), one copy each.
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (half) group_sync(qi);                 // the first copy has read the stage
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t* o = &v[32 * half + 4 * c];
+              st_shared16(srow + ((c ^ (r & 7)) << 4), __float_as_uint(__uint_as_float(o[0]) * inv),
+                          __float_as_uint(__uint_as_float(o[1]) * inv), __float_as_uint(__uint_as_float(o[2]) * inv),
+                          __float_as_uint(__uint_as_float(o[3]) * inv));
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(R.part_o + (((int64_t)split * R.n_q + row) * P.num_heads + h) * HD);
-#pragma unroll
-            for (int i = 0; i < HD / 4; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
-                                   __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
-            R.part_lse[((int64_t)split * R.n_q + row) * P.num_heads + h] = m_fin + __log2f(l);
+            fence_proxy_async();
+            group_sync(qi);
+            if (issuer) {
+              tma_store_3d(&P.part_map[rq], stage, h * HD + 32 * half, q0 + qi * BM, split);
+              bulk_commit();
+              bulk_wait_read();                       // before the stage is reused or goes away
+            }
           }
         }
       }
@@ -1005,6 +1071,31 @@ cudaError_t launch_impl(const TcBatchArgs& b, EncodeTiledFn enc, cudaStream_t st
     if (!d.maps || d.n_q < 0 || d.n_splits < 1 || d.q_row0 < 0 || d.q_row0 + d.n_q > b.rows)
       return cudaErrorInvalidValue;
     TcRequest& q = P.req[r];
+    if (d.n_q > 0) {
+      // Output tile maps: one split writes bf16 / f16 rows of `out`; several
+      // write fp32 partials [n_splits][n_q][H * D].  Both use 128-byte rows
+      // in the 128-byte swizzle, as staged by the epilogue.
+      CUresult mr;
+      if (d.n_splits == 1) {
+        cuuint64_t odims[2] = {(cuuint64_t)b.num_heads * HD, (cuuint64_t)d.n_q};
+        cuuint64_t ostr[1] = {row_bytes};
+        cuuint32_t obox[2] = {HD, BM};
+        mr = enc(&P.out_map[r], b.dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                 static_cast<char*>(b.out) + (size_t)d.q_row0 * row_bytes, odims, ostr, obox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      } else {
+        const cuuint64_t prow = (cuuint64_t)b.num_heads * HD * 4;
+        cuuint64_t pdims[3] = {(cuuint64_t)b.num_heads * HD, (cuuint64_t)d.n_q, (cuuint64_t)d.n_splits};
+        cuuint64_t pstr[2] = {prow, prow * (cuuint64_t)d.n_q};
+        cuuint32_t pbox[3] = {32, BM, 1};
+        cuuint32_t pestr[3] = {1, 1, 1};
+        mr = enc(&P.part_map[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d.part_o, pdims, pstr, pbox, pestr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      }
+      if (mr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     P.cache_map[r] = d.maps->cache;
     for (int u = 0; u < 4; ++u) P.cache_map_u[r][u] = d.maps->cache_u[u];
     q.tiles = d.tiles;
