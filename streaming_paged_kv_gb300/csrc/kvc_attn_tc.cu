@@ -102,7 +102,8 @@ constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + STAGES * TILE_BYTES;
 // Dual-mode hand-off from softmax group 1 to group 0: [128 rows][max, sum, flag].
 constexpr uint32_t OFF_XCH = OFF_BAR + 256;
-constexpr uint32_t SMEM_BYTES = OFF_XCH + BM * 3 * 4 + 1024;  // + alignment slack
+constexpr uint32_t OFF_STATE = OFF_XCH + BM * 3 * 4;            // CtaState
+constexpr uint32_t SMEM_BYTES = OFF_STATE + 32 + 1024;  // + alignment slack
 
 // ------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -134,46 +135,63 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait.  Returns false when the CTA is (or becomes) aborted.
-struct Guard {
-  volatile int* abort_flag;   // shared
-  int32_t* status;            // global
+// CTA state of the bounded waits, in shared memory: the abort flag, the status
+// word of the CTA's request and the wait budget.  A wait passes only its
+// barrier; the slow path (rare) reads the rest from here.
+struct CtaState {
+  int abort_flag;
+  int pad;
+  int32_t* status;
   long long budget;
 };
 
-__device__ __noinline__ void raise_abort(const Guard& g, int where) {
-  *g.abort_flag = 1;
-  if (atomicCAS(g.status, 0, 1) == 0) {
-    g.status[1] = where;
-    g.status[2] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+__device__ __forceinline__ CtaState* cta_state() {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  return reinterpret_cast<CtaState*>(smem + OFF_STATE);
+}
+
+__device__ __noinline__ void raise_abort(int where) {
+  CtaState* cs = cta_state();
+  *reinterpret_cast<volatile int*>(&cs->abort_flag) = 1;
+  if (atomicCAS(cs->status, 0, 1) == 0) {
+    cs->status[1] = where;
+    cs->status[2] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
   }
   __threadfence();
 }
 
 // Checked builds: a tile outside its cache records the failure (code, where,
 // value) and aborts the CTA through the same path as a timed-out wait.
-__device__ __noinline__ void raise_bounds(const Guard& g, int where, int value) {
-  *g.abort_flag = 1;
-  record_bounds(g.status, where, value);
+__device__ __noinline__ void raise_bounds(int where, int value) {
+  CtaState* cs = cta_state();
+  *reinterpret_cast<volatile int*>(&cs->abort_flag) = 1;
+  record_bounds(cs->status, where, value);
 }
 
-__device__ __forceinline__ bool wait_bar(const Guard& g, uint64_t* bar, uint32_t parity, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait.  Returns false when the CTA is (or becomes) aborted.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, int where) {
+  CtaState* cs = cta_state();
   const long long t0 = clock64();
   while (true) {
-    if (*g.abort_flag) return false;
+    if (*reinterpret_cast<volatile int*>(&cs->abort_flag)) return false;
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > g.budget) {
-      raise_abort(g, where);
+    if (clock64() - t0 > cs->budget) {
+      raise_abort(where);
       return false;
     }
   }
 }
 
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, where);
+}
+
 // Bounded wait whose outcome is the same for all 32 lanes of the warp (the
 // warp-collective tcgen05.ld / st that follow need a converged warp).
-__device__ __forceinline__ bool wait_bar_warp(const Guard& g, uint64_t* bar, uint32_t parity, int where) {
-  const bool ok = wait_bar(g, bar, parity, where);
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, int where) {
+  const bool ok = wait_bar(bar, parity, where);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -423,6 +441,77 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
 
 // ------------------------------------------------------------------ kernel
 template <int OFF, int N>
+__device__ __forceinline__ void tmem_st16_at(uint32_t taddr, const uint32_t (&v)[N]);
+
+// Rare path of a score tile whose row sum left [2^-64, 2^64] (or is not a
+// number): S is still intact in TMEM.  Rereads it, moves the reference of the
+// overflowing rows to their max, stores the redone P over S's first 64
+// columns, and rescales O once the previous P V product has completed.
+// Returns false when that wait gave up.
+template <bool BF16>
+__device__ __noinline__ bool rescue_tile(uint32_t S_, uint32_t O_, float sl2, bool moved, int j,
+                                         uint64_t* prev_done, uint32_t prev_parity, float* m_ref_io, uint64_t* ta_out,
+                                         uint64_t* tb_out, float* alpha_out) {
+  uint32_t v[BN];
+  tmem_ld32(S_, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+  tmem_ld32(S_ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+  tmem_ld32(S_ + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+  tmem_ld32(S_ + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < BN; c += 8) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      m4[u] = fmax3(m4[u], __uint_as_float(v[c + 2 * u]), __uint_as_float(v[c + 2 * u + 1]));
+  }
+  const float m_ref = *m_ref_io;
+  const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+  const float m_new = moved ? mt : m_ref;
+  const float alpha = j > 0 ? ex2(m_ref - m_new) : 0.f;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  const uint64_t negm2 = f2_pack(-m_new, -m_new);
+  uint32_t pk[BN / 2];
+  uint64_t ta = 0, tb = 0;
+#pragma unroll
+  for (int t = 0; t < BN / 2; ++t) {
+    const uint64_t x = ffma2(f2_pack(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1])), sl2x2, negm2);
+    const float p0 = ex2(f2_lo(x)), p1 = ex2(f2_hi(x));
+    if (t & 1) tb = fadd2(tb, f2_pack(p0, p1));
+    else ta = fadd2(ta, f2_pack(p0, p1));
+    pk[t] = pack2<BF16>(p0, p1);
+  }
+  tmem_st16_at<0>(S_, pk);
+  tmem_st16_at<16>(S_ + 16, pk);
+  tmem_st16_at<32>(S_ + 32, pk);
+  tmem_st16_at<48>(S_ + 48, pk);
+  bool ok = true;
+  if (j > 0) {
+    ok = wait_bar_warp(prev_done, prev_parity, 8);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < HD / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(O_ + cc * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+        tmem_st32(O_ + cc * 32, o);
+      }
+    }
+  }
+  *m_ref_io = m_new;
+  *ta_out = ta;
+  *tb_out = tb;
+  *alpha_out = alpha;
+  return ok;
+}
+
+template <int OFF, int N>
 __device__ __forceinline__ void tmem_st16_at(uint32_t taddr, const uint32_t (&v)[N]) {
   static_assert(OFF + 16 <= N, "range");
   tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(&v[OFF]));
@@ -494,7 +583,8 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
   uint64_t* drain = o_done + 3 * QT;               // [2] one per MMA-issuing warp
   uint64_t* never = drain + 2;                    // signalled by nothing (timeout test)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  CtaState* cstate = reinterpret_cast<CtaState*>(smem + OFF_STATE);
+  volatile int* abort_flag = &cstate->abort_flag;
   static_assert((1 + 2 * STAGES + 3 * NBUF + 3 * QT + 3) * 8 + 8 <= 256, "barrier area");
 
   const int warp = threadIdx.x >> 5;
@@ -524,7 +614,6 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
   const KvTile* tiles = R.tiles;
   const CUtensorMap* cache_map = &P.cache_map[rq];
   const CUtensorMap* maps_u = P.cache_map_u[rq];
-  Guard g{abort_flag, R.status, P.wait_budget};
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -542,6 +631,8 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
     mbar_init(&drain[1], 1);
     mbar_init(never, 1);
     *abort_flag = 0;
+    cstate->status = R.status;
+    cstate->budget = P.wait_budget;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -574,7 +665,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
       }
       for (int j = 0; j < n; ++j) {
         const int st = j % STAGES;
-        if (j >= STAGES && !wait_bar_warp(g, &kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
+        if (j >= STAGES && !wait_bar_warp(&kv_empty[st], ((j / STAGES) + 1) & 1, 1)) break;
         const KvTile tile = tiles[t0 + j];
         const int plane = (R.page_base + tile.page) * 2;
         const int units1 = (tile.rows + 7) >> 3;        // 8-row units of the first segment
@@ -584,7 +675,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
              (tile.page2 < 0 ? tile.rows2 != 0
                              : (tile.page2 >= R.max_pages || tile.row0_2 < 0 || tile.rows2 < 1 ||
                                 units1 * 8 + tile.rows2 > BN || tile.row0_2 + tile.rows2 > R.page_size)))) {
-          if (leader) raise_bounds(g, 401, t0 + j);
+          if (leader) raise_bounds(401, t0 + j);
           __syncwarp();
           break;
         }
@@ -651,14 +742,14 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
         constexpr uint32_t IDESC_S = idesc_f16(BM, BN, BF16, false);
         const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
-        ok = wait_bar_warp(g, q_full, 0, 2);
+        ok = wait_bar_warp(q_full, 0, 2);
         for (int k = 0; ok && k < n_s; ++k) {
           if (i == 0) {
-            ok = wait_bar_warp(g, &kv_full[st], (kv_par >> st) & 1, 3);
+            ok = wait_bar_warp(&kv_full[st], (kv_par >> st) & 1, 3);
             kv_par ^= 1u << st;
           }
           if (ok && k >= NBUF) {
-            ok = wait_bar_warp(g, &buf_free[b], (buf_par >> b) & 1, 4);
+            ok = wait_bar_warp(&buf_free[b], (buf_par >> b) & 1, 4);
             buf_par ^= 1u << b;
           }
           if (!ok) break;
@@ -687,15 +778,15 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
         constexpr uint32_t IDESC_O = idesc_f16(BM, HD, BF16, true);
         const uint64_t dV0 = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
         uint32_t p_par = 0;
-        ok = !P.stall_test || wait_bar_warp(g, never, 0, 12);
+        ok = !P.stall_test || wait_bar_warp(never, 0, 12);
         for (int k = 0, j = 0; ok && k < n_s; ++k) {
           if (i == 0) {
             // V(j) landed (already true in practice: S(k) needed K(j) of the same copy).
-            ok = wait_bar_warp(g, &kv_full[st], (kv_par >> st) & 1, 3);
+            ok = wait_bar_warp(&kv_full[st], (kv_par >> st) & 1, 3);
             kv_par ^= 1u << st;
           }
           if (ok) {
-            ok = wait_bar_warp(g, &p_full[b], (p_par >> b) & 1, 5);
+            ok = wait_bar_warp(&p_full[b], (p_par >> b) & 1, 5);
             p_par ^= 1u << b;
           }
           if (!ok) break;
@@ -761,7 +852,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
       const int k = j * groups + qi, b = k % NBUF;
       const int rows_valid = rows_next;
       if (j + 1 < n_g) rows_next = tile_rows(t0 + (dual ? k + 2 : j + 1));   // prefetch for the next tile
-      ok = wait_bar_warp(g, &s_full[b], (k / NBUF) & 1, 6);
+      ok = wait_bar_warp(&s_full[b], (k / NBUF) & 1, 6);
       if (!ok) break;
       tc_fence_after();
       const uint32_t S_ = lane_base + buf_col(b);
@@ -814,49 +905,19 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
       const bool moved = !(tsum <= 0x1p64f) || (j == 0 && !(tsum >= 0x1p-64f));
       float alpha = 1.f;
       if (__any_sync(0xffffffffu, moved)) {
-        // Rare: S is still intact in TMEM (P is stored below).  Reread it, move
-        // the reference of the overflowing rows to their max, redo P, and
-        // rescale O (once the previous P V product has completed) and the sums.
-        tmem_ld32_at<0>(S_, v);
-        tmem_ld32_at<32>(S_ + 32, v);
-        tmem_ld32_at<64>(S_ + 64, v);
-        tmem_ld32_at<96>(S_ + 96, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < BN; c += 8) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            m4[u] = fmax3(m4[u], __uint_as_float(v[c + 2 * u]), __uint_as_float(v[c + 2 * u + 1]));
-        }
-        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-        const float m_new = moved ? mt : m_ref;
-        alpha = j > 0 ? ex2(m_ref - m_new) : 0.f;    // nothing accumulated before the first tile
-        exponentiate(m_new);
-        if (j > 0) {
-          ok = wait_bar_warp(g, &o_done[3 * qi + (j - 1) % 3], ((j - 1) / 3) & 1, 8);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll 1
-          for (int cc = 0; cc < HD / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(O_ + cc * 32, o);
-            tmem_wait_ld();
-            reg_fence(o);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-            tmem_st32(O_ + cc * 32, o);
-          }
-        }
-        m_ref = m_new;
+        // Rare (out of line, to keep its registers out of this loop): the
+        // previous product into this accumulator is j - 1 (waited for only
+        // when j > 0).
+        ok = rescue_tile<BF16>(S_, O_, sl2, moved, j, &o_done[3 * qi + (j + 2) % 3], ((j - 1) / 3) & 1, &m_ref, &ta,
+                               &tb, &alpha);
+        if (!ok) break;
+      } else {
+        // P as 16-bit pairs over S's first 64 columns.
+        tmem_st16_at<0>(S_, pk);
+        tmem_st16_at<16>(S_ + 16, pk);
+        tmem_st16_at<32>(S_ + 32, pk);
+        tmem_st16_at<48>(S_ + 48, pk);
       }
-      // P as 16-bit pairs over S's first 64 columns.
-      tmem_st16_at<0>(S_, pk);
-      tmem_st16_at<16>(S_ + 16, pk);
-      tmem_st16_at<32>(S_ + 32, pk);
-      tmem_st16_at<48>(S_ + 48, pk);
       const uint64_t alpha2 = f2_pack(alpha, alpha);
       la = ffma2(la, alpha2, ta);
       lb = ffma2(lb, alpha2, tb);
@@ -869,7 +930,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
       // the row.  In dual mode group 1 hands its row max and sum to group 0
       // through shared memory, and group 0 combines both halves (group 1's O
       // sits in the same TMEM lanes) before writing.
-      bool good = ok && wait_bar_warp(g, &o_done[3 * qi + (n_g - 1) % 3], ((n_g - 1) / 3) & 1, 9);
+      bool good = ok && wait_bar_warp(&o_done[3 * qi + (n_g - 1) % 3], ((n_g - 1) / 3) & 1, 9);
       float l = (f2_lo(la) + f2_hi(la)) + (f2_lo(lb) + f2_hi(lb));
       float m_fin = m_ref, w0 = 1.f, w1 = 0.f;
       if (dual) {
@@ -884,7 +945,7 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
           good = false;                              // group 0 writes the row
         } else if (good && xr[2] == 0.f) {
           const int n_g1 = n / 2;                    // group 1's tiles
-          good = wait_bar_warp(g, &o_done[3 + (n_g1 - 1) % 3], ((n_g1 - 1) / 3) & 1, 9);
+          good = wait_bar_warp(&o_done[3 + (n_g1 - 1) % 3], ((n_g1 - 1) / 3) & 1, 9);
           const float m1 = xr[0], l1 = xr[1];
           m_fin = fmaxf(m_ref, m1);
           w0 = ex2(m_ref - m_fin);
