@@ -43,12 +43,22 @@
 // O only after the previous P V product has completed) only when a tile's row
 // sum would exceed 2^64 (or, on the first tile, fall below 2^-64): the
 // relative precision of P, O and the sums does not depend on the reference,
-// only their range does, so most tiles need no row max at all.
+// only their range does, so most tiles need no row max at all; that rare
+// path is a separate, non-inlined function, which keeps its registers out of
+// the softmax loop.
+//
+// K/V tiles are loaded with an L2 evict-first policy, so that the split-KV
+// partials stay in L2 for the merge kernel.  The epilogue stages each query
+// tile's normalised rows in shared memory (the tile's own Q area) and writes
+// them with TMA stores: the bf16 / f16 output, or the fp32 partials (their
+// log2-sum-exp goes out with plain stores).
 //
 // Every mbarrier wait is bounded: when a wait runs out, the thread records
 // the fact in the status word, raises a CTA-wide abort flag, and every role
 // skips its remaining work, drains its own in-flight copies / MMAs (again
-// with a bound), frees TMEM and returns.
+// with a bound), frees TMEM and returns.  The flag, the status pointer and
+// the budget live in shared memory, read only by the out-of-line slow path
+// of a wait.
 
 #include "kvc_internal.h"
 
