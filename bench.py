@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="s518",
-                   help="s518 (default, the streamed metric), s224, phase1, batch224, win518 or camcache")
+                   help="s518 (default, the streamed metric), s224, defer, phase1, batch224, win518 or camcache")
     p.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     p.add_argument("--splits", type=int, default=0, help="tuning: force the KV split count (0 = the library's choice)")
     p.add_argument("--qtiles", type=int, default=0,
@@ -621,6 +621,121 @@ def run_windowed(args, rank, world):
     }
 
 
+DEFER_METRIC = ("keyframe + deferred-eviction stream frames/s (12-layer paged attn, 224x224; each frame after the "
+                "scale frames provisional, then accepted or rolled back); attention vs GB300 roofline")
+
+
+def run_defer(args, rank, world):
+    """The keyframe + deferred-eviction stream: after the scale frames every
+    frame is appended with eviction deferred, planned and attended on every
+    layer, then accepted (execute_deferred_eviction) or rolled back by a
+    seeded coin.  The frames before the timed ones run untimed with the same
+    decisions, so that the timed frames see the stream's own cache state."""
+    import torch
+    from streaming_paged_kv_gb300 import build
+    build.build()
+    from streaming_paged_kv_gb300 import kvc
+    from streaming_paged_kv_gb300.inputs import keyframe_decisions
+    from streaming_paged_kv_gb300.workloads import WORKLOADS, schedule
+    w = WORKLOADS["defer"]
+    if args.layers:
+        w = w.with_(num_layers=args.layers)
+    if args.frames:
+        w = w.with_(n_frames=args.frames)
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    events = list(schedule(w, keyframe_decisions(args.seed + rank, w.wid, w.n_frames)))
+    K = max(1, min(args.steps or 60, len(events) - max(args.warmup, 3)))
+    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits, args.qtiles)
+    c, L = st.c, w.num_layers
+    book = kvc.PagedKVCache(1, w.num_heads, w.head_dim, w.page_size, w.dtype, w.scale_frames,
+                            w.sliding_window, w.headroom, w.max_total_frames, device=None)
+
+    def frame(f, kind, count=None):
+        prov = kind in ("accept", "reject")
+        if prov:
+            c.set_defer_eviction(True)
+            book.set_defer_eviction(True)
+        book.append_frame(0)
+        book.evict_frames(0)
+        if count is not None:
+            s_ = book.stats(0)
+            count.append(w.page_size * (s_["scale_pages"] + s_["live_pages"]) + s_["special_tokens"])
+        for b in range(L):
+            q, k, v = st.inputs(f, b)
+            c.append_frame(b, k, v)
+            c.evict_frames(b)
+            if b == 0:
+                c.plan()
+            c.run(b, q, st.out[b])
+        if kind == "accept":
+            for b in range(L):
+                c.execute_deferred_eviction(b)
+            book.execute_deferred_eviction(0)
+        elif kind == "reject":
+            for b in range(L):
+                c.rollback_last_frame(b)
+            book.rollback_last_frame(0)
+        if prov:
+            c.set_defer_eviction(False)
+            book.set_defer_eviction(False)
+
+    for f, kind in events[:len(events) - K]:     # untimed, the warm-up frames included
+        frame(f, kind)
+    torch.cuda.synchronize()
+    kvc.kvc_get_counters(c.h, reset=True)
+    c.set_option(kvc.KVC_OPT_TIMING, 1)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    nkv = []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for f, kind in events[len(events) - K:]:
+        frame(f, kind, nkv)
+    ev1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms, total_frames = aggregate(ev0.elapsed_time(ev1), K, world, dev)
+    launches, attn_launches, attn_ms = kvc.kvc_get_counters(c.h, reset=True)
+    c.set_option(kvc.KVC_OPT_TIMING, 0)
+    if kvc.kvc_device_status(c.h, c._stream()) != 0:
+        raise RuntimeError("device status")
+    T, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
+    flops = sum(L * 4.0 * T * n * H * D for n in nkv)
+    bytes_alg = sum(L * (2.0 * n * H * D * 2 + 2.0 * T * H * D * 2) for n in nkv)
+    roof = attn_roofline(roof_bound(flops, bytes_alg), flops, bytes_alg, attn_ms, attn_launches, ms,
+                         "paged attention (kvc_run attention launch)")
+    roof["outside_attn_ms_per_step"] = (ms - attn_ms) / K
+    roof["launch_shape"] = dict(zip(("q_tiles", "splits"), kvc.kvc_get_launch_shape(c.h)))
+    kinds = [kind for _, kind in events[len(events) - K:]]
+    book.close()
+    del st
+    torch.cuda.empty_cache()
+    return {
+        "metric": DEFER_METRIC, "value": total_frames / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
+        "steps": K, "warmup": len(events) - K, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"defer: 224x224 keyframe + deferred-eviction stream, {L} layers, H={H}, D={D}, "
+                               f"page_size={w.page_size}, {w.n_frames} frames; timed = the last {K} frames "
+                               f"({kinds.count('accept')} accepted, {kinds.count('reject')} rolled back)",
+                   "l2": "no flush: a frame reads the visible K/V of 12 layers (about 1 GB) between two launches of a layer, above L2",
+                   "parallelism": f"replicas x{world} (independent streams, no collective)"},
+        "roofline": roof,
+        "attn_tflops": roof["attn_tflops"],
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+
+
 PHASE1_METRIC = ("Phase-1 batch prefill frames/s (8 scale frames x 1005 tokens, dense bidirectional, "
                  "24-layer paged attn, 518x378); attn TFLOP/s vs GB300 roofline")
 
@@ -905,13 +1020,15 @@ def run_extra(args, rank, world):
     """The other workloads' numbers, measured in the same run after the
     default one: the windowed long stream (one whole window from its clean
     start, with per-frame latency percentiles), the last 60 frames of the
-    224x224 stream, 8 batched 224x224 streams (one attention launch per
-    layer), the trunk's cache beside the camera head's own cache, and the
-    Phase-1 prefill of the scale frames."""
+    224x224 stream, the last 60 frames of the keyframe + deferred-eviction
+    stream, 8 batched 224x224 streams (one attention launch per layer), the
+    trunk's cache beside the camera head's own cache, and the Phase-1 prefill
+    of the scale frames."""
     import torch
     extra = {}
     plans = (("win518", run_windowed, {"steps": None, "warmup": 5}),
              ("s224", run_ours, {"workload": "s224", "steps": 60, "warmup": 5, "no_e2e": True}),
+             ("defer", run_defer, {"steps": 60, "warmup": 5}),
              ("batch224", run_batch224, {"steps": 60, "warmup": 5}),
              ("camcache", run_paired, {"steps": 20, "warmup": 5}),
              ("phase1", run_phase1, {"steps": 10, "warmup": 3}))
@@ -1062,9 +1179,9 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    if args.workload in ("phase1", "batch224", "win518", "camcache"):
+    if args.workload in ("phase1", "batch224", "win518", "camcache", "defer"):
         res = {"phase1": run_phase1, "batch224": run_batch224, "win518": run_windowed,
-               "camcache": run_paired}[args.workload](args, rank, world)
+               "camcache": run_paired, "defer": run_defer}[args.workload](args, rank, world)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if world > 1:
