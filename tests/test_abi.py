@@ -86,4 +86,18 @@ def test_geometry_and_launch_shape_accessors(kvc):
     assert g.block_bytes == 101 * g.page_bytes == 101 * 2 * 999 * 16 * 64 * 2
     c = kvc.PagedKVCache(1, 2, 32, 16, "f32", 2, 4, 2, 16, device=None)
     assert kvc.kvc_get_launch_shape(c.h) == (0, 0)      # no attention launched
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_get_plan_tiles(c.h)                      # no plan yet
+    for _ in range(3):
+        c.append_frame(0)
+        c.evict_frames(0)
+    c.plan()
+    # A bookkeeping-only handle plans for the CUDA-core kernel (64-row tiles,
+    # one page per tile): 3 patch pages of 16 rows, and the 3 frames' special
+    # rows on two special pages of 2 frames each (12 and 6 rows).
+    assert c.plan_ranges()[2] == [16, 16, 16, 12, 6]
+    assert kvc.kvc_get_plan_tiles(c.h) == (5, False)
+    c.clean()
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_get_plan_tiles(c.h)                      # clean drops the plan
     c.close()
