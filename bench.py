@@ -339,7 +339,7 @@ def run_ours(args, rank, world):
             bytes_alg += w.num_layers * (2.0 * nkv * H * D * 2 + 2.0 * n_q * H * D * 2)
     book.close()
     kvc.kvc_get_counters(st.c.h, reset=True)
-    st.c.set_option(kvc.KVC_OPT_TIMING, 1)
+    st.c.set_option(kvc.KVC_OPT_TIMING, w.num_layers)   # one timed launch per frame
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -444,7 +444,7 @@ def run_paired(args, rank, world):
     book.close()
     for st in streams:
         kvc.kvc_get_counters(st.c.h, reset=True)
-        st.c.set_option(kvc.KVC_OPT_TIMING, 1)
+        st.c.set_option(kvc.KVC_OPT_TIMING, st.w.num_layers)   # one timed launch per frame
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -559,7 +559,7 @@ def run_windowed(args, rank, world):
     torch.cuda.synchronize()
     timed = [(f, kind) for f, kind in schedule(w.with_(n_frames=w.window_frames))][:K + 1]
     kvc.kvc_get_counters(c.h, reset=True)
-    c.set_option(kvc.KVC_OPT_TIMING, 1)
+    c.set_option(kvc.KVC_OPT_TIMING, L)   # one timed launch per frame
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -684,7 +684,7 @@ def run_defer(args, rank, world):
         frame(f, kind)
     torch.cuda.synchronize()
     kvc.kvc_get_counters(c.h, reset=True)
-    c.set_option(kvc.KVC_OPT_TIMING, 1)
+    c.set_option(kvc.KVC_OPT_TIMING, L)   # one timed launch per frame
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -779,7 +779,7 @@ def run_phase1(args, rank, world):
         step()
     torch.cuda.synchronize()
     kvc.kvc_get_counters(c.h, reset=True)
-    c.set_option(kvc.KVC_OPT_TIMING, 1)
+    c.set_option(kvc.KVC_OPT_TIMING, L)   # one timed launch per step
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -879,7 +879,7 @@ def run_batch224(args, rank, world):
     bytes_alg = K * L * B * (2.0 * nkv * H * D * 2 + 2.0 * T * H * D * 2)
     h0 = streams[0].c
     kvc.kvc_get_counters(h0.h, reset=True)
-    h0.set_option(kvc.KVC_OPT_TIMING, 1)
+    h0.set_option(kvc.KVC_OPT_TIMING, L)   # one timed launch per step
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)

@@ -295,7 +295,12 @@ enum {
   KVC_OPT_ATTN_KERNEL = 1, /* 0 auto, 1 CUDA-core kernel, 2 tensor-core (tcgen05) kernel */
   KVC_OPT_NUM_SPLITS = 2,  /* 0 auto, else the number of KV splits (<= max_kv_splits)     */
   KVC_OPT_WAIT_BUDGET = 3, /* bounded-wait budget in SM clock cycles; 0 => default (~2 s) */
-  KVC_OPT_TIMING = 4,      /* 1: time every attention launch with CUDA events            */
+  KVC_OPT_TIMING = 4,      /* N >= 1: time attention launches with CUDA events on their
+                              stream -- every one (N = 1), or one in every N: the (N/2)-th
+                              of each group of N launches counted from this call, whose
+                              time then counts N times in kvc_get_counters (a bench whose
+                              step makes N launches of one shape times one per step);
+                              0: off                                                         */
   KVC_OPT_STALL_TEST = 5,  /* test only, 1: the tensor-core kernel first waits on a barrier
                               that nothing signals, so its bounded wait runs out and the run
                               reports KVC_ERR_DEVICE_TIMEOUT (no output is written)           */

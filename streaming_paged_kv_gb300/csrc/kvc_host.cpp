@@ -177,6 +177,8 @@ struct kvc_handle {
   bool opt_pack = true;
   long long wait_budget = 0;
   bool timing = false;
+  int32_t timing_every = 1;         // time one attention launch in every timing_every
+  int64_t timing_count = 0;         // attention launches since timing was set
   int stall_test = 0;
   // Counters.
   int64_t launches = 0, attn_launches = 0;
@@ -294,13 +296,22 @@ Shape choose_shape(const kvc_handle* h, int kernel, int32_t n_q) {
   return Shape{1, best_s};
 }
 
+// Whether the attention launch about to be made is a timed one: with timing
+// set to N, the (N / 2)-th launch of every group of N since it was set.
+bool timed_launch(kvc_handle* h) {
+  if (!h->timing) return false;
+  const int64_t i = h->timing_count++;
+  return i % h->timing_every == h->timing_every / 2;
+}
+
 void record_timing(kvc_handle* h, int which, cudaStream_t st) {
   // which 0: start, 1: stop of the current pair.
   int i = h->ev_next;
   if (which == 0 && h->ev_used[i]) {
     float ms = 0.f;
     cudaEventSynchronize(h->ev[2 * i + 1]);
-    if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) == cudaSuccess) h->attn_ms += ms;
+    if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) == cudaSuccess)
+      h->attn_ms += (double)ms * h->timing_every;
     h->ev_used[i] = false;
   }
   cudaEventRecord(h->ev[2 * i + which], st);
@@ -316,7 +327,8 @@ void drain_timing(kvc_handle* h) {
     if (!h->ev_used[i]) continue;
     float ms = 0.f;
     cudaEventSynchronize(h->ev[2 * i + 1]);
-    if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) == cudaSuccess) h->attn_ms += ms;
+    if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) == cudaSuccess)
+      h->attn_ms += (double)ms * h->timing_every;
     h->ev_used[i] = false;
   }
 }
@@ -704,7 +716,8 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
   const int splits = shape.splits;
   const kvc::AttnArgs a = attn_args(h, block, Q, out, n_q, splits);
   cudaStream_t st = (cudaStream_t)stream;
-  if (h->timing) record_timing(h, 0, st);
+  const bool timed = timed_launch(h);
+  if (timed) record_timing(h, 0, st);
   cudaError_t err;
   if (kernel == 2) {
     kvc::TcBatchArgs tb = tc_batch_header(h, Q, out, n_q);
@@ -719,7 +732,7 @@ int kvc_run(kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q,
     h->last_qt = 0;
     h->last_splits = splits;
   }
-  if (h->timing) record_timing(h, 1, st);
+  if (timed) record_timing(h, 1, st);
   if (err != cudaSuccess) return KVC_ERR_CUDA;
   ++h->launches;
   ++h->attn_launches;
@@ -803,9 +816,10 @@ int kvc_run_batch(kvc_handle* const* hs, const int32_t* blocks, int32_t count, c
     tb.req[r] = tc_request(hs[r], blocks[r], qo_indptr[r], n_q, s_r > 0 ? s_r : 1);
   }
   cudaStream_t st = (cudaStream_t)stream;
-  if (h0->timing) record_timing(h0, 0, st);
+  const bool timed = timed_launch(h0);
+  if (timed) record_timing(h0, 0, st);
   cudaError_t err = kvc::launch_attn_tc(tb, st);
-  if (h0->timing) record_timing(h0, 1, st);
+  if (timed) record_timing(h0, 1, st);
   if (err != cudaSuccess) return KVC_ERR_CUDA;
   ++h0->launches;
   ++h0->attn_launches;
@@ -1002,6 +1016,7 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
       h->stall_test = (int)value;
       return KVC_OK;
     case KVC_OPT_TIMING:
+      if (value < 0 || value > 0x7fffffff) return KVC_ERR_INVALID_ARG;
       if (value && !h->ev) {
         if (!h->device) return KVC_ERR_NO_DEVICE;
         cudaEvent_t* ev = (cudaEvent_t*)std::calloc(2 * kEventPairs, sizeof(cudaEvent_t));
@@ -1018,7 +1033,10 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
         h->ev = ev;
         h->ev_used = used;
       }
+      drain_timing(h);                          // earlier samples keep their own scale
       h->timing = value != 0;
+      h->timing_every = value > 1 ? (int32_t)value : 1;
+      h->timing_count = 0;
       return KVC_OK;
     default:
       return KVC_ERR_INVALID_ARG;
