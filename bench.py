@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--splits", type=int, default=0, help="tuning: force the KV split count (0 = the library's choice)")
     p.add_argument("--qtiles", type=int, default=0,
                    help="tuning: 128-row query tiles per CTA of the tensor-core kernel (0 = the library's choice)")
+    p.add_argument("--pdl", type=int, default=1,
+                   help="tuning: 1 programmatic dependent launch between the library's kernels (default), 0 off")
     p.add_argument("--pool", type=int, default=4, help="distinct input frames per layer")
     p.add_argument("--batch", type=int, default=8, help="streams of --workload batch224")
     p.add_argument("--seed", type=int, default=0)
@@ -189,7 +191,7 @@ class ClockSampler:
 class Stream:
     """One device stream of the workload through the library."""
 
-    def __init__(self, kvc, w, pool, seed, kernel, dev, splits=0, qtiles=0):
+    def __init__(self, kvc, w, pool, seed, kernel, dev, splits=0, qtiles=0, pdl=1):
         import torch
         from streaming_paged_kv_gb300.inputs import k_head_scale
         self.torch, self.kvc, self.w = torch, kvc, w
@@ -202,6 +204,8 @@ class Stream:
             self.c.set_option(kvc.KVC_OPT_NUM_SPLITS, splits)
         if qtiles:
             self.c.set_option(kvc.KVC_OPT_QUERY_TILES, qtiles)
+        if not pdl:
+            self.c.set_option(kvc.KVC_OPT_PDL, 0)
         T, H, D = w.tokens_per_frame, w.num_heads, w.head_dim
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
@@ -318,7 +322,7 @@ def run_ours(args, rank, world):
     W = args.warmup
     K = max(1, min(K, w.n_frames))
     W = max(0, min(W, w.n_frames - K))
-    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits, args.qtiles)
+    st = Stream(kvc, w, args.pool, args.seed + rank, args.kernel, dev, args.splits, args.qtiles, args.pdl)
     st.fast_forward(w.n_frames - K - W)
     for _ in range(W):
         st.step()

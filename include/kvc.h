@@ -308,12 +308,16 @@ enum {
                               cost model picks tiles and splits per launch), 1 (both softmax
                               warp groups share one tile, taking alternate KV tiles), 2 (one
                               warp group per tile)                                           */
-  KVC_OPT_PACK_TILES = 7   /* tensor-core kernel: 1 (default) packs the KV tiles across page
+  KVC_OPT_PACK_TILES = 7,  /* tensor-core kernel: 1 (default) packs the KV tiles across page
                               boundaries in units of 8 rows -- a page's last tile is filled
                               with the next page's first rows -- when every visible page but
                               the last has at least 113 rows (otherwise the plan keeps one
                               page per tile); 0 never packs.  Takes effect at the next
                               kvc_plan.                                                      */
+  KVC_OPT_PDL = 8          /* 1 (default): launch with programmatic dependent launch, so that
+                              each kernel of the library is set up while the kernel before it
+                              in the stream drains (it touches no memory before that kernel has
+                              completed); 0: ordinary launches                              */
 };
 int kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
 

@@ -570,6 +570,7 @@ static_assert(sizeof(TcLaunch<kTcMaxBatch>) <= 32764, "kernel parameter space");
 template <bool BF16, int MAXB>
 __global__ void __launch_bounds__(REG_BOUND_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + OFF_Q;
@@ -652,6 +653,9 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // Barriers and TMEM are set up while the previous kernel of the stream may
+  // still drain; nothing below runs before it has completed.
+  pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1196,8 +1200,7 @@ cudaError_t launch_impl(const TcBatchArgs& b, EncodeTiledFn enc, cudaStream_t st
     if (e != cudaSuccess) return e;
     configured_smem[which] = true;
   }
-  kernel<<<(unsigned)ctas, NUM_THREADS, SMEM_BYTES, stream>>>(P);
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3((unsigned)ctas), dim3(NUM_THREADS), SMEM_BYTES, stream, b.pdl != 0, P);
 }
 
 }  // namespace

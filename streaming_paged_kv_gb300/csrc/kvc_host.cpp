@@ -175,6 +175,7 @@ struct kvc_handle {
   int opt_splits = 0;
   int opt_qtiles = 0;
   bool opt_pack = true;
+  bool opt_pdl = true;
   long long wait_budget = 0;
   bool timing = false;
   int32_t timing_every = 1;         // time one attention launch in every timing_every
@@ -358,6 +359,7 @@ int check_run(const kvc_handle* h, int32_t block, const void* Q, const void* out
 
 kvc::AttnArgs attn_args(const kvc_handle* h, int32_t block, const void* Q, void* out, int32_t n_q, int splits) {
   kvc::AttnArgs a;
+  a.pdl = h->opt_pdl ? 1 : 0;
   a.q = Q;
   a.out = out;
   a.cache = h->cache + (size_t)block * h->g.block_bytes;
@@ -381,6 +383,7 @@ kvc::AttnArgs attn_args(const kvc_handle* h, int32_t block, const void* Q, void*
 kvc::TcBatchArgs tc_batch_header(const kvc_handle* h, const void* Q, void* out, int32_t rows) {
   kvc::TcBatchArgs tb;
   std::memset(&tb, 0, sizeof(tb));
+  tb.pdl = h->opt_pdl ? 1 : 0;
   tb.q = Q;
   tb.out = out;
   tb.rows = rows;
@@ -547,7 +550,7 @@ int kvc_append_frame(kvc_handle* h, int32_t block, const void* K, const void* V,
     char* cache_block = h->cache + (size_t)block * h->g.block_bytes;
     cudaError_t err = kvc::launch_append(cache_block, K, V, page, sp_page, sp_slot, cam_page, cam_slot,
                                          h->cfg.page_size, h->g.row_bytes, h->g.max_pages,
-                                         (int32_t*)(h->ws + h->g.L.status), (cudaStream_t)stream);
+                                         (int32_t*)(h->ws + h->g.L.status), (cudaStream_t)stream, h->opt_pdl);
     if (err != cudaSuccess) return KVC_ERR_CUDA;
     ++h->launches;
   }
@@ -687,7 +690,7 @@ int kvc_plan(kvc_handle* h, kvc_stream stream) {
   if (n_tiles > h->g.L.max_tiles) return KVC_ERR_INVALID_ARG;
   a.pack = pack ? 1 : 0;
   if (h->device) {
-    cudaError_t err = kvc::launch_plan(a, h->ws, h->g.L, (cudaStream_t)stream);
+    cudaError_t err = kvc::launch_plan(a, h->ws, h->g.L, (cudaStream_t)stream, h->opt_pdl);
     if (err != cudaSuccess) return KVC_ERR_CUDA;
     ++h->launches;
   }
@@ -1001,6 +1004,10 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value) {
     case KVC_OPT_QUERY_TILES:
       if (value < 0 || value > 2) return KVC_ERR_INVALID_ARG;
       h->opt_qtiles = (int)value;
+      return KVC_OK;
+    case KVC_OPT_PDL:
+      if (value < 0 || value > 1) return KVC_ERR_INVALID_ARG;
+      h->opt_pdl = value != 0;
       return KVC_OK;
     case KVC_OPT_PACK_TILES:
       if (value < 0 || value > 1) return KVC_ERR_INVALID_ARG;

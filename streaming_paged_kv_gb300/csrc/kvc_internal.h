@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #ifdef __CUDACC__
 #define KVC_HD __host__ __device__
 #else
@@ -35,6 +37,34 @@ __device__ inline void record_bounds(int32_t* status, int32_t where, int32_t val
   __threadfence();
 }
 #endif
+#ifdef __CUDACC__
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream drains:
+// pdl_wait() returns once that kernel has completed and its memory operations
+// are visible (at once for a kernel launched the ordinary way), and
+// pdl_trigger() lets the next kernel of the stream be launched early.  Every
+// kernel of the library calls pdl_wait() before it touches global memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kernel` on `st`, with programmatic stream serialization when `pdl`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#endif
+
 constexpr int kMaxPatchPages = 1024;   // bound on P (the patch pool), kernel-argument sized
 
 // Device plan written by the plan kernel into the workspace.
@@ -139,15 +169,16 @@ struct AttnArgs {
   float sm_scale_log2;    // sm_scale * log2(e)
   long long wait_budget;  // clock cycles per bounded wait
   int32_t stall_test;     // 1: wait once on a barrier nothing signals (timeout test)
+  int32_t pdl;            // launch with programmatic stream serialization
 };
 
 // kvc_kernels.cu
 cudaError_t launch_append(void* cache_block, const void* K, const void* V, int32_t page,
                           int32_t special_page, int32_t special_slot, int32_t camera_page,
                           int32_t camera_slot, int32_t page_size, int64_t row_bytes, int32_t max_pages,
-                          int32_t* status, cudaStream_t stream);
+                          int32_t* status, cudaStream_t stream, bool pdl);
 cudaError_t launch_plan(const PlanArgs& a, void* workspace, const WorkspaceLayout& L,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool pdl);
 cudaError_t launch_attn_simt(const AttnArgs& a, int dtype, cudaStream_t stream);
 cudaError_t launch_merge(const AttnArgs& a, int dtype, cudaStream_t stream);
 int simt_tile_rows(int head_dim);
@@ -179,6 +210,7 @@ struct TcBatchArgs {
   int32_t rows, num_heads, head_dim, dtype, stall_test, count;
   int32_t num_sms;        // of the device: decides whether a launch has several waves
   int32_t q_tiles;        // 128-row query tiles per CTA: 2, or 1 (both softmax groups on one tile)
+  int32_t pdl;            // launch with programmatic stream serialization
   float sm_scale_log2;
   long long wait_budget;
   TcRequestDesc req[kTcMaxBatch];

@@ -31,6 +31,8 @@ __global__ void append_kernel(char* __restrict__ cache_block, const char* __rest
                               int32_t special_slot, int32_t camera_page, int32_t camera_slot,
                               int32_t page_size, int64_t row_bytes, int32_t max_pages,
                               int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();
   const int32_t T = kNumSpecial + page_size;
   if (KVC_CHECKED && (page < 0 || page >= max_pages || special_page < 0 || special_page >= max_pages ||
                       special_slot < 0 || special_slot + kNumSpecial > page_size ||
@@ -117,6 +119,8 @@ __device__ PlanEntry plan_entry(const PlanArgs& a, int32_t e, int32_t u) {
 // the tile has room left, the next entry's first rows.
 __global__ void plan_kernel(const __grid_constant__ PlanArgs a, char* __restrict__ ws,
                             WorkspaceLayout L) {
+  pdl_trigger();
+  pdl_wait();
   const int32_t tr = a.tile_rows;
   const int32_t u = a.pack ? kPackUnitRows : tr;     // unit of the tile offsets
   const int32_t per_tile = tr / u;                   // units per tile
@@ -193,6 +197,8 @@ constexpr int kSimtThreads = 128;
 template <typename T, int D, int BN>
 __global__ void __launch_bounds__(kSimtThreads)
 attn_simt_kernel(const AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sK[BN][D];
   __shared__ float sV[BN][D];
   const int h = blockIdx.y;
@@ -287,6 +293,8 @@ attn_simt_kernel(const AttnArgs a) {
 // loads in flight.
 template <typename T, int D>
 __global__ void merge_kernel(const AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int TPR = D / 4;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t rh = gid / TPR;                      // row * H + head
@@ -332,8 +340,7 @@ template <typename T, int D>
 cudaError_t simt_dispatch(const AttnArgs& a, cudaStream_t st) {
   constexpr int BN = D >= 128 ? 32 : 64;
   dim3 grid((a.n_q + kSimtThreads - 1) / kSimtThreads, a.num_heads, a.n_splits);
-  attn_simt_kernel<T, D, BN><<<grid, kSimtThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(attn_simt_kernel<T, D, BN>, grid, dim3(kSimtThreads), 0, st, a.pdl != 0, a);
 }
 
 template <typename T>
@@ -353,13 +360,13 @@ cudaError_t merge_by_dim(const AttnArgs& a, cudaStream_t st) {
   // D / 4 threads per (row, head)
   const unsigned blocks = (unsigned)((n_rh * (a.head_dim / 4) + threads - 1) / threads);
   if (blocks == 0) return cudaSuccess;
+  const bool pdl = a.pdl != 0;
   switch (a.head_dim) {
-    case 32: merge_kernel<T, 32><<<blocks, threads, 0, st>>>(a); break;
-    case 64: merge_kernel<T, 64><<<blocks, threads, 0, st>>>(a); break;
-    case 128: merge_kernel<T, 128><<<blocks, threads, 0, st>>>(a); break;
+    case 32: return launch_kernel(merge_kernel<T, 32>, dim3(blocks), dim3(threads), 0, st, pdl, a);
+    case 64: return launch_kernel(merge_kernel<T, 64>, dim3(blocks), dim3(threads), 0, st, pdl, a);
+    case 128: return launch_kernel(merge_kernel<T, 128>, dim3(blocks), dim3(threads), 0, st, pdl, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -369,22 +376,19 @@ int simt_tile_rows(int head_dim) { return head_dim >= 128 ? 32 : 64; }
 cudaError_t launch_append(void* cache_block, const void* K, const void* V, int32_t page,
                           int32_t special_page, int32_t special_slot, int32_t camera_page,
                           int32_t camera_slot, int32_t page_size, int64_t row_bytes, int32_t max_pages,
-                          int32_t* status, cudaStream_t stream) {
+                          int32_t* status, cudaStream_t stream, bool pdl) {
   const int64_t row16 = row_bytes / 16;
   const int threads = row16 >= 128 ? 128 : (int)((row16 + 31) / 32 * 32);
   const unsigned rows = (unsigned)(kNumSpecial + page_size + (camera_page >= 0 ? 1 : 0));
   dim3 grid((unsigned)((row16 + threads - 1) / threads), 2u * rows);
-  append_kernel<<<grid, threads, 0, stream>>>(static_cast<char*>(cache_block),
-                                             static_cast<const char*>(K), static_cast<const char*>(V),
-                                             page, special_page, special_slot, camera_page, camera_slot,
-                                             page_size, row_bytes, max_pages, status);
-  return cudaGetLastError();
+  return launch_kernel(append_kernel, grid, dim3(threads), 0, stream, pdl, static_cast<char*>(cache_block),
+                       static_cast<const char*>(K), static_cast<const char*>(V), page, special_page,
+                       special_slot, camera_page, camera_slot, page_size, row_bytes, max_pages, status);
 }
 
 cudaError_t launch_plan(const PlanArgs& a, void* workspace, const WorkspaceLayout& L,
-                        cudaStream_t stream) {
-  plan_kernel<<<1, 256, 0, stream>>>(a, static_cast<char*>(workspace), L);
-  return cudaGetLastError();
+                        cudaStream_t stream, bool pdl) {
+  return launch_kernel(plan_kernel, dim3(1), dim3(256), 0, stream, pdl, a, static_cast<char*>(workspace), L);
 }
 
 cudaError_t launch_attn_simt(const AttnArgs& a, int dtype, cudaStream_t stream) {

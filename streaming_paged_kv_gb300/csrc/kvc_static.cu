@@ -187,6 +187,7 @@ extern "C" int kvc_paged_attention_static(const void* cache_block, int32_t dtype
   if (cudaGetLastError() != cudaSuccess) return KVC_ERR_CUDA;
 
   AttnArgs a;
+  a.pdl = 0;
   a.q = Q;
   a.out = out;
   a.cache = cache_block;

@@ -35,6 +35,7 @@ ERRORS = {
 KVC_OPT_ATTN_KERNEL, KVC_OPT_NUM_SPLITS, KVC_OPT_WAIT_BUDGET, KVC_OPT_TIMING, KVC_OPT_STALL_TEST = 1, 2, 3, 4, 5
 KVC_OPT_QUERY_TILES = 6
 KVC_OPT_PACK_TILES = 7
+KVC_OPT_PDL = 8
 
 try:
     _DEBUG_EVERY = max(0, int(os.environ.get("KVC_DEBUG", "0") or 0))   # see PagedKVCache.plan
