@@ -50,3 +50,32 @@ def test_sampled_timing_matches_every_launch(kvc):
         c.set_option(kvc.KVC_OPT_TIMING, -1)
     assert kvc.kvc_device_status(c.h, c._stream()) == 0
     c.close()
+
+
+def test_pdl_off_gives_identical_outputs(kvc):
+    """KVC_OPT_PDL only changes how the kernels are launched: outputs with and
+    without programmatic dependent launch are bit-identical (several layers,
+    so that append, plan, attention and merge follow each other)."""
+    from streaming_paged_kv_gb300.inputs import frame_qkv
+    outs = []
+    for pdl in (1, 0):
+        c = kvc.PagedKVCache(3, 16, 64, 256, "bf16", max_total_frames=64)
+        c.set_option(kvc.KVC_OPT_PDL, pdl)
+        res = []
+        for f in range(12):
+            for b in range(3):
+                q, k, v = frame_qkv(9, 2, f, b, 256, 16, 64)
+                c.append_frame(b, k.cuda(), v.cuda())
+                c.evict_frames(b)
+                if b == 0:
+                    c.plan()
+                out = torch.empty_like(q.cuda())
+                c.run(b, q.cuda(), out)
+                res.append(out)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status(c.h, c._stream()) == 0
+        outs.append(torch.stack(res).cpu())
+        c.close()
+    assert torch.equal(outs[0], outs[1])
+    with pytest.raises(kvc.KvcError):
+        kvc.PagedKVCache(1, 16, 64, 256, "bf16", max_total_frames=64).set_option(kvc.KVC_OPT_PDL, 2)
