@@ -16,6 +16,11 @@ U(0.5, 2) factor); frame f of layer b uses pool entry (f + b) mod pool.  Every
 layer's visible K/V (~340 MB at full context) is larger than L2, so no flush is
 needed between steps.
 
+The attention launches' duration (for the roofline) comes from CUDA events
+that the library records on the launching stream around one attention launch
+per step (the middle layer's; every layer of a step launches the same shape),
+so that the measurement adds two events per step instead of two per layer.
+
 Output: one JSON line (see the keys below).  ``--impl reference`` times the CPU
 oracle instead, on a bounded sample of the same workload.
 """

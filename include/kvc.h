@@ -323,8 +323,9 @@ int kvc_set_option(kvc_handle* h, int32_t option, int64_t value);
 
 /* Counters since creation (or the last reset with reset != 0): kernel
  * launches made by the library, attention launches, and -- with
- * KVC_OPT_TIMING -- the summed device time of the attention launches in
- * milliseconds (synchronises the pending timing events). */
+ * KVC_OPT_TIMING -- the summed device time of the timed attention launches in
+ * milliseconds, each counted N times when one launch in every N is timed
+ * (synchronises the pending timing events). */
 int kvc_get_counters(kvc_handle* h, int64_t* kernel_launches, int64_t* attn_launches,
                      double* attn_ms, int32_t reset);
 
