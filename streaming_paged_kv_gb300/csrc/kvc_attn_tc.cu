@@ -885,14 +885,16 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
         for (; c < BN; c += 8) tmem_st8(S_ + c, ninf);
         tmem_wait_st();
       }
+      // The row's 128 scores: the first half is waited for, the second half's
+      // loads are in flight while the first half is exponentiated.
       uint32_t v[BN];
       tmem_ld32_at<0>(S_, v);
       tmem_ld32_at<32>(S_ + 32, v);
-      tmem_ld32_at<64>(S_ + 64, v);
-      tmem_ld32_at<96>(S_ + 96, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
+      for (int c = 0; c < BN / 2; ++c) asm volatile("" : "+r"(v[c])::"memory");
+      tmem_ld32_at<64>(S_ + 64, v);
+      tmem_ld32_at<96>(S_ + 96, v);
       // P = 2^(s * scale - m_ref) against the running reference, held in
       // registers until the row sum shows that it is usable.  The reference
       // only has to keep P and the sums finite -- their relative precision
@@ -901,19 +903,22 @@ attn_tc_kernel(const __grid_constant__ TcLaunch<MAXB> P) {
       // more in log2 units), or -- on the first tile -- falls below 2^-64.
       uint32_t pk[BN / 2];
       uint64_t ta = 0, tb = 0;
-      auto exponentiate = [&](float m) {
-        const uint64_t negm2 = f2_pack(-m, -m);
-        ta = tb = 0;
+      {
+        const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
 #pragma unroll
         for (int t = 0; t < BN / 2; ++t) {
+          if (t == BN / 4) {
+            tmem_wait_ld();                            // the second half of the scores
+#pragma unroll
+            for (int c = BN / 2; c < BN; ++c) asm volatile("" : "+r"(v[c])::"memory");
+          }
           const uint64_t x = ffma2(f2_pack(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1])), sl2x2, negm2);
           const float p0 = ex2(f2_lo(x)), p1 = ex2(f2_hi(x));
           if (t & 1) tb = fadd2(tb, f2_pack(p0, p1));
           else ta = fadd2(ta, f2_pack(p0, p1));
           pk[t] = pack2<BF16>(p0, p1);
         }
-      };
-      exponentiate(m_ref);
+      }
       const float tsum = (f2_lo(ta) + f2_hi(ta)) + (f2_lo(tb) + f2_hi(tb));
       // The first tile also moves the reference when its sum underflows.
       const bool moved = !(tsum <= 0x1p64f) || (j == 0 && !(tsum >= 0x1p-64f));
