@@ -272,12 +272,20 @@ def kernel_code_hash(path):
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
-def profiled_traffic(alg_bytes_per_launch):
-    """DRAM bytes per attention launch from the committed ncu summary, scaled to
-    this run's average launch by algorithmic bytes -- or None when the kernel
-    code differs from the one the counters were taken on."""
+# The committed ncu summary whose DRAM counters stand for each workload's
+# attention launch (same kernel and launch shape, one layer at a late frame).
+TRAFFIC_PROFILES = {"s518": "attn_tc_s518_l1f200_full.md", "s224": "attn_tc_s224_l1f200_full.md"}
+
+
+def profiled_traffic(alg_bytes_per_launch, workload_name="s518"):
+    """DRAM bytes per attention launch from the workload's committed ncu
+    summary, scaled to this run's average launch by algorithmic bytes -- or None
+    when there is no summary for the workload or the kernel code differs from
+    the one the counters were taken on."""
     import re
-    prof = os.path.join(ROOT, "profiles", "attn_tc_s518_l1f200_full.md")
+    if workload_name not in TRAFFIC_PROFILES:
+        return None
+    prof = os.path.join(ROOT, "profiles", TRAFFIC_PROFILES[workload_name])
     src = os.path.join(ROOT, "streaming_paged_kv_gb300", "csrc", "kvc_attn_tc.cu")
     try:
         text = open(prof, encoding="utf-8").read()
@@ -379,7 +387,7 @@ def run_ours(args, rank, world):
     bound = roof_bound(flops, bytes_alg)
     roofline = attn_roofline(bound, flops, bytes_alg, attn_ms, attn_launches, ms,
                              "paged attention (kvc_run attention launch)",
-                             profiled_traffic(bytes_alg / max(attn_launches, 1)) if w.name == "s518" else None)
+                             profiled_traffic(bytes_alg / max(attn_launches, 1), w.name))
     roofline["outside_attn_ms_per_step"] = (ms - attn_ms) / K
     roofline["launch_shape"] = dict(zip(("q_tiles", "splits"), kvc.kvc_get_launch_shape(st.c.h)))
     res = {
@@ -1014,7 +1022,7 @@ def run_e2e(args, kvc, w, dev, rank, world, K, W):
 def compact(r):
     """The headline fields of another workload's bench line."""
     roof = r.get("roofline", {})
-    keep = ("bound", "achieved", "peak", "unit", "frac", "frac_sustained", "step_frac", "attn_tflops",
+    keep = ("bound", "achieved", "peak", "unit", "frac", "traffic", "frac_sustained", "step_frac", "attn_tflops",
             "launch_ms", "outside_attn_ms_per_step", "launch_shape")
     out = {"metric": r["metric"], "value": r["value"], "unit": r["unit"], "steps": r["steps"],
            "ms_per_step": r["ms_per_step"], "workload": r["config"]["workload"],
